@@ -1,0 +1,119 @@
+"""CPU oracle for segmented reduction over offset-delimited (CSR) segments.
+
+TEST INFRASTRUCTURE ONLY.  The product path never imports this package: only
+``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference leg of
+``bench.py`` may.  It shares no code with the CUDA library.
+
+Two independent implementations live here:
+
+* ``seg_reduce``: the sequential C loop in ``seg_oracle.c`` (built with gcc,
+  called through ctypes) -- the oracle proper, fast enough for the full
+  synthetic workloads.
+* ``brute.seg_reduce``: a pure-Python restatement with Python integers and
+  ``math.fsum`` for tiny inputs, used to pin the C oracle.
+
+Semantics (GPUSegmentedReduction "Contract"; graph-reduce README "API",
+"Method" and "Correctness"): segment ``s`` reduces rows
+``[offsets[s], offsets[s+1])`` of ``values`` (shape ``[N]`` or ``[N, F]``,
+reduced over dimension 0); ops ``sum``, ``min``, ``max`` for uint32 / int32 /
+float32 and ``mean`` for float32; ``min``/``max`` also give the absolute source
+row (ties to the lower row); empty segments give 0 and arg -1.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "seg_oracle.c")
+_LIBDIR = os.path.join(_HERE, "lib")
+_LIB = os.path.join(_LIBDIR, "libsegoracle.so")
+
+# Codes private to seg_oracle.c.
+_DT = {np.dtype(np.uint32): 0, np.dtype(np.int32): 1, np.dtype(np.float32): 2}
+_OFF = {np.dtype(np.uint32): 0, np.dtype(np.int64): 1}
+_OP = {"sum": 0, "min": 1, "max": 2, "mean": 3}
+_ERR = {-1: "bad argument", -2: "offsets not nondecreasing within [0, N]",
+        -3: "mean is defined for float32 only"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_source(src: str, dst: str) -> str:
+    """gcc -O2 without fast-math or FMA contraction, as a shared library."""
+    tmp = dst + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", "-o", tmp, src]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, dst)
+    return dst
+
+
+def build(force: bool = False) -> str:
+    """Compile seg_oracle.c into lib/libsegoracle.so."""
+    os.makedirs(_LIBDIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    return compile_source(_SRC, _LIB)
+
+
+def load_library(path: str):
+    """ctypes handle of a compiled oracle library (the default one, or a
+    deliberately broken copy that a test builds to check the pins)."""
+    lib = ctypes.CDLL(path)
+    lib.oracle_seg_reduce.restype = ctypes.c_int
+    lib.oracle_seg_reduce.argtypes = [
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_void_p]
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = load_library(_LIB)
+    return _lib
+
+
+def seg_reduce(values, offsets, op: str, with_arg: bool = True, lib=None):
+    """Reduce ``values`` ([N] or [N, F]) over the segments that ``offsets`` ([S+1]) delimits.
+
+    Returns ``out`` (shape ``[S]`` or ``[S, F]``, dtype of ``values``) for
+    sum / mean, and ``(out, arg)`` (arg int64, same shape) for min / max
+    when ``with_arg``.
+    """
+    values = np.ascontiguousarray(values)
+    offsets = np.ascontiguousarray(offsets)
+    if values.dtype not in _DT:
+        raise TypeError(f"unsupported values dtype {values.dtype}")
+    if offsets.dtype not in _OFF:
+        raise TypeError(f"unsupported offsets dtype {offsets.dtype}")
+    if op not in _OP:
+        raise ValueError(f"unknown op {op!r}")
+    if values.ndim not in (1, 2) or offsets.ndim != 1 or offsets.shape[0] < 1:
+        raise ValueError("values must be [N] or [N, F]; offsets must be [S+1]")
+    n = values.shape[0]
+    f = 1 if values.ndim == 1 else values.shape[1]
+    s = offsets.shape[0] - 1
+    oshape = (s,) if values.ndim == 1 else (s, f)
+    out = np.zeros(oshape, dtype=values.dtype)
+    want_arg = with_arg and op in ("min", "max")
+    arg = np.zeros(oshape, dtype=np.int64) if want_arg else None
+    lib = _load() if lib is None else lib
+    rc = lib.oracle_seg_reduce(
+        values.ctypes.data, _DT[values.dtype], f, n,
+        offsets.ctypes.data, _OFF[offsets.dtype], s, _OP[op],
+        out.ctypes.data, arg.ctypes.data if want_arg else None)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the input: {_ERR.get(rc, rc)}")
+    return (out, arg) if want_arg else out
+

@@ -1,0 +1,66 @@
+"""Pure-Python brute force of segmented reduction, for tiny inputs only.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  It is written
+independently of ``seg_oracle.c`` so that each pins the other: Python integers
+reduced modulo 2**32 for integer sums, ``math.fsum`` (the correctly rounded
+sum) for float sums, and an explicit loop that keeps the first row holding
+the extreme for min / max (graph-reduce README, "Method": ties go to the
+lower row).  Segment semantics follow GPUSegmentedReduction, "What is an
+offset-delimited segment?" and "Contract".
+"""
+from __future__ import annotations
+
+import math
+import struct
+
+
+def _to_f32(x: float) -> float:
+    return struct.unpack("<f", struct.pack("<f", x))[0]
+
+
+def _wrap(x: int, signed: bool) -> int:
+    x %= 1 << 32
+    if signed and x >= 1 << 31:
+        x -= 1 << 32
+    return x
+
+
+def seg_reduce(values, offsets, op: str, kind: str, feat=None):
+    """``values``: list of rows (each row a list of F numbers), ``offsets``: list of ints.
+
+    ``kind`` is "u32", "s32" or "f32"; ``feat`` (F) is needed when there
+    are no rows.  Returns (out, arg): lists of rows;
+    arg rows hold -1 for empty segments and for sum / mean.
+    """
+    S = len(offsets) - 1
+    F = feat if feat is not None else (len(values[0]) if values else 1)
+    out, arg = [], []
+    for s in range(S):
+        b, e = offsets[s], offsets[s + 1]
+        orow, arow = [], []
+        for f in range(F):
+            col = [values[r][f] for r in range(b, e)]
+            if not col:
+                orow.append(0.0 if kind == "f32" else 0)
+                arow.append(-1)
+                continue
+            if op in ("sum", "mean"):
+                if kind == "f32":
+                    total = _to_f32(math.fsum(col))
+                    if op == "mean":
+                        total = _to_f32(total / _to_f32(float(len(col))))
+                    orow.append(total)
+                else:
+                    orow.append(_wrap(sum(int(x) for x in col), kind == "s32"))
+                arow.append(-1)
+            else:
+                best_i = 0
+                for i in range(1, len(col)):
+                    better = col[i] < col[best_i] if op == "min" else col[i] > col[best_i]
+                    if better:
+                        best_i = i
+                orow.append(col[best_i])
+                arow.append(b + best_i)
+        out.append(orow)
+        arg.append(arow)
+    return out, arg
