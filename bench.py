@@ -1,0 +1,384 @@
+"""Benchmark: segmented reduction over CSR offsets on one GB300 (or N replicas).
+
+A step is one pass of the whole path over the workload: every (dtype, op)
+case the workload lists (the scalar-bulk workload: uint32 / int32 / float32
+x sum / min+arg / max+arg), each one seg_reduce call = one kernel launch.
+
+value        algorithmic bytes of the step / summed CUDA-event kernel time,
+             inputs resident in HBM, L2 flushed (a 2 x L2 write) before
+             every call, outside the events.
+e2e          the same bytes / time of a step that copies its inputs from
+             pinned host memory, runs the calls and copies the outputs back.
+roofline     the reduction kernel against the measured HBM copy bandwidth.
+cpu_baseline the C oracle on the host cores (one thread) over the same cases.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "segmented-reduce effective HBM GB/s and % of GB300 peak; segments/s (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["ptx.cuh", "seg_common.cuh", "seg_rows.cuh", "seg_scalar.cuh", "seg_pick.cuh", "api.cu"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "segmented_reduction_csr_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(config: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; otherwise None."""
+    p = os.path.join(ROOT, "profiles", f"seg_reduce_{config}_traffic.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+    except Exception:
+        return None
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cases_of(w: W.Workload):
+    return [(k, op) for k, op in w.cases]
+
+
+def step_bytes(w: W.Workload) -> int:
+    return sum(W.workload_bytes(w, k, op) for k, op in cases_of(w))
+
+
+def run_reference(args, w: W.Workload):
+    """The oracle timed on the host cores over the same cases (a bounded sample
+    per step when the full workload would take too long)."""
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    cases = cases_of(w)
+    offsets = w.offsets
+    # bound one step to about 2 s of CPU: prefix of segments
+    t0 = time.perf_counter()
+    for k, op in cases[:1]:
+        oracle.seg_reduce(w.values[k], offsets, op)
+    one = time.perf_counter() - t0
+    est_step = one * len(cases)
+    frac = min(1.0, 2.0 / max(est_step, 1e-9))
+    S = w.num_segments
+    s_take = max(1, int(S * frac))
+    sub = offsets[: s_take + 1]
+    rows = int(sub[-1]) - int(sub[0])
+    sample_bytes = sum(W.algorithmic_bytes(rows, w.feat, s_take, offsets.dtype.itemsize, op)
+                       for _, op in cases)
+    for _ in range(args.warmup):
+        for k, op in cases:
+            oracle.seg_reduce(w.values[k], sub, op)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        for k, op in cases:
+            oracle.seg_reduce(w.values[k], sub, op)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    gbs = sample_bytes * args.steps / tot / 1e9
+    sample = (f"first {s_take} of {S} segments ({rows} rows), all {len(cases)} cases per step"
+              if s_take < S else f"whole workload, all {len(cases)} cases per step")
+    return {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32/s32/f32" if w.feat == 1 else "f32",
+        "data": "synthetic", "config": config_of(args, w),
+        "segments_per_s": s_take * len(cases) * args.steps / tot,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def config_of(args, w):
+    return {"workload": f"{w.name}: " + {
+        "tiny": "1,000 segments, ~7.5K rows, uint32 offsets",
+        "bulk": "1,000,000 segments, geometric lengths mean 16 (~16M rows), int64 offsets",
+        "mp": "1,000,000 rows x 64 float32 into 10,000 segments, int64 indptr",
+        "skewed": "64M float32 rows, 1M segments, Zipf(1.5) + 4 giants > 5M, 20% empty",
+        "large": "10M rows x 128 float32, 100,000 power-law segments",
+    }[w.name], "segments": w.num_segments, "rows": w.num_rows, "features": w.feat,
+        "cases": [f"{k}:{op}" for k, op in cases_of(w)],
+        "l2": "flushed before every timed call (2 x L2 write), outside the events"}
+
+
+def run_ours(args, w: W.Workload):
+    import torch
+
+    import segmented_reduction_csr_gb300 as sr
+    from segmented_reduction_csr_gb300 import build as srbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    srbuild.build()
+    lib = sr.load_library()
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint32:
+            return torch.from_numpy(a.view(np.int32)).to(dev).view(torch.uint32)
+        return torch.from_numpy(a).to(dev)
+
+    cases = cases_of(w)
+    dvals = {k: to_dev(v) for k, v in w.values.items()}
+    doff = to_dev(w.offsets)
+    outs = {}
+    for k, op in cases:
+        shape = (w.num_segments,) if w.feat == 1 else (w.num_segments, w.feat)
+        o = torch.empty(shape, dtype=dvals[k].dtype, device=dev)
+        a = torch.empty(shape, dtype=torch.int64, device=dev) if op in ("min", "max") else None
+        outs[(k, op)] = (o, a)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(k, op):
+        o, a = outs[(k, op)]
+        sr.seg_reduce(dvals[k], doff, op, out=o, out_arg=a, with_arg=a is not None)
+
+    for _ in range(args.warmup):
+        for k, op in cases:
+            flush.zero_()
+            call(k, op)
+    torch.cuda.synchronize(dev)
+    assert sr.device_status(stream) == 0
+
+    # ---- device-resident timing --------------------------------------------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps * len(cases))]
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    n = 0
+    for _ in range(args.steps):
+        for k, op in cases:
+            flush.zero_()
+            ev[n][0].record(stream)
+            call(k, op)
+            ev[n][1].record(stream)
+            n += 1
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    per_call = [s.elapsed_time(e) for s, e in ev]             # ms
+    kernel_ms = sum(per_call)
+    if world > 1:
+        t = torch.tensor([kernel_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        kernel_ms = float(t.item())
+    assert sr.device_status(stream) == 0
+    bytes_step = step_bytes(w)
+    value = world * bytes_step * args.steps / (kernel_ms * 1e-3) / 1e9
+    by_case = {}
+    for idx, (k, op) in enumerate(cases * args.steps):
+        by_case.setdefault((k, op), []).append(per_call[idx])
+    breakdown = []
+    for k, op in cases:
+        ms = statistics.median(by_case[(k, op)])
+        b = W.workload_bytes(w, k, op)
+        breakdown.append({"case": f"{k}:{op}", "us_median": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
+                          "bytes": b})
+
+    # ---- end to end through host buffers ------------------------------------
+    host_vals = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int32) if v.dtype == np.uint32 else v)).pin_memory()
+                 for k, v in w.values.items()}
+    host_off = torch.from_numpy(w.offsets).pin_memory()
+    host_outs = {key: (torch.empty(o.shape, dtype=o.dtype if o.dtype != torch.uint32 else torch.int32).pin_memory(),
+                       torch.empty(a.shape, dtype=torch.int64).pin_memory() if a is not None else None)
+                 for key, (o, a) in outs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_vals.values()) + host_off.numel() * host_off.element_size()
+    d2h = sum(o.numel() * o.element_size() + (a.numel() * 8 if a is not None else 0)
+              for o, a in host_outs.values())
+
+    def e2e_step():
+        for k, hv in host_vals.items():
+            dst = dvals[k].view(torch.int32) if dvals[k].dtype == torch.uint32 else dvals[k]
+            dst.copy_(hv, non_blocking=True)
+        doff.copy_(host_off, non_blocking=True)
+        for k, op in cases:
+            call(k, op)
+        for key, (ho, ha) in host_outs.items():
+            o, a = outs[key]
+            ho.copy_(o.view(torch.int32) if o.dtype == torch.uint32 else o, non_blocking=True)
+            if ha is not None:
+                ha.copy_(a, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = world * bytes_step * args.steps / (e2e_ms * 1e-3) / 1e9
+
+    # ---- CPU baseline (rank 0, N == 1 only) --------------------------------
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        ref = run_reference(argparse.Namespace(steps=1, warmup=0, gpus=1), w)
+        cpu = ref["cpu_baseline"]
+
+    peak, peak_kind = measured_peak()
+    achieved = bytes_step * args.steps / (sum(per_call) * 1e-3) / 1e9
+    traffic = profile_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": kernel_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "u32/s32/f32" if w.feat == 1 else "f32", "data": "synthetic",
+        "config": config_of(args, w),
+        "pct_of_peak": 100.0 * value / world / peak, "peak_gbs": peak, "peak_kind": peak_kind,
+        "pct_of_8tbs": 100.0 * value / world / 8000.0,
+        "segments_per_s": world * w.num_segments * len(cases) * args.steps / (kernel_ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "segred::seg_reduce_kernel (all instantiations of the step)",
+                     "peak_note": f"{peak_kind} HBM copy bandwidth"},
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * len(cases),
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+        "breakdown": breakdown,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="bulk", choices=W.NAMES)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    w = W.make(args.config)
+    if args.impl == "reference":
+        line = run_reference(args, w)
+    else:
+        line = run_ours(args, w)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,147 @@
+/*
+ * seg_reduce.h -- C ABI of libsegreduce, a segmented reduction over
+ * offset-delimited (CSR indptr) segments for NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  GPUSegmentedReduction (luma.gl API reference), sections
+ * "What is an offset-delimited segment?" and "Contract": segment s owns the
+ * half-open row range [offsets[s], offsets[s+1]); S segments take S+1
+ * offsets; repeated offsets are empty segments and an empty segment produces
+ * zero; offsets[0] may be non-zero and rows outside [offsets[0], offsets[S])
+ * are ignored.  graph-reduce README (HF kernels hub), sections "API",
+ * "Method" and "Correctness": values may be a row tensor [N, F] reduced
+ * over dimension 0 (one result per segment and column); min and max also
+ * report the source row, with ties going to the lower row; mean is the
+ * segment sum divided by the segment length and is 0 for an empty segment;
+ * the arg of an empty segment is -1.
+ *
+ * Numerics.  uint32 / sint32 sums wrap modulo 2^32.  uint32 compares
+ * unsigned, sint32 signed, float32 by IEEE '<' / '>' (-0.0 ties with +0.0,
+ * so the lower row and its bits win; NaN inputs give unspecified results).
+ * float32 sums are not in row order, but the order is a pure function of
+ * (num_values, F, S, offsets) and the GPU's SM count, so repeated calls are
+ * bitwise identical; the error is below 1e-5 * sum(|x|) + 1e-6 per output.
+ * mean = (float)sum / (float)length, rounded to nearest.
+ *
+ * Memory.  Every pointer argument except `out_arg` may be NULL only when
+ * num_segments == 0.  All data pointers are device pointers owned by the
+ * caller, on the device that is current for the calling host thread; the
+ * library keeps no reference after the call returns.  Scratch space is owned
+ * by the library: one small buffer per (device, stream), allocated on first
+ * use (stream-ordered), grown when needed and kept until process exit.
+ * Outputs must not overlap inputs.
+ *
+ * Asynchrony.  seg_reduce enqueues work on `stream` and returns without
+ * synchronising and without reading any device memory on the host.  Errors
+ * that the host can see (argument checks, launch failures) are returned
+ * before or at launch; a device-side error (a bounded wait that ran out)
+ * is recorded in a per-device status word that seg_reduce_device_status
+ * reads.
+ */
+#ifndef SEG_REDUCE_H
+#define SEG_REDUCE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *seg_stream_t;
+
+typedef enum { SEG_U32 = 0, SEG_S32 = 1, SEG_F32 = 2 } seg_dtype_t;
+typedef enum { SEG_OFF_U32 = 0, SEG_OFF_I64 = 1 } seg_offset_dtype_t;
+typedef enum { SEG_SUM = 0, SEG_MIN = 1, SEG_MAX = 2, SEG_MEAN = 3 } seg_op_t;
+
+typedef enum {
+    SEG_OK = 0,
+    SEG_ERR_INVALID_ARGUMENT = 1, /* a null pointer, a bad enum, a negative size, misaligned data */
+    SEG_ERR_UNSUPPORTED = 2,      /* mean on integer values, F above SEG_MAX_FEATURES */
+    SEG_ERR_OUT_OF_MEMORY = 3,    /* the scratch buffer could not be allocated */
+    SEG_ERR_CUDA = 4,             /* a CUDA runtime call or a launch failed */
+    SEG_ERR_DEVICE_TIMEOUT = 5    /* a device-side bounded wait ran out (see seg_reduce_device_status) */
+} seg_status_t;
+
+/* Largest F (columns per row) that seg_reduce accepts. */
+#define SEG_MAX_FEATURES 2048
+
+/*
+ * seg_reduce -- out[s, f] = op over rows r in [offsets[s], offsets[s+1]) of values[r, f].
+ *
+ *   values        device, [num_values, F] row-major, element type `dtype`,
+ *                 aligned to 4 bytes (16 bytes enables the vectorised
+ *                 row path when F is a multiple of 4).
+ *   dtype         SEG_U32, SEG_S32 or SEG_F32.
+ *   F             columns per row, 1 <= F <= SEG_MAX_FEATURES; F == 1 is the
+ *                 scalar vector case.
+ *   num_values    rows in `values` (N >= 0).  Offsets are clamped to [0, N]
+ *                 on the device, so malformed offsets never read out of bounds.
+ *   offsets       device, [num_segments + 1], SEG_OFF_U32 (uint32) or
+ *                 SEG_OFF_I64 (int64), aligned to its element size.
+ *                 Precondition (not checked, as in the luma contract):
+ *                 nondecreasing and within [0, N].  If it does not hold the
+ *                 results are unspecified but no memory outside the
+ *                 arguments is touched.
+ *   num_segments  S >= 0.  S == 0 returns SEG_OK and launches nothing.
+ *   op            SEG_SUM, SEG_MIN, SEG_MAX, or SEG_MEAN (float32 only,
+ *                 otherwise SEG_ERR_UNSUPPORTED).
+ *   out           device, [S, F], element type `dtype`, aligned to 4 bytes.
+ *   out_arg       device, [S, F] int64, or NULL.  For SEG_MIN / SEG_MAX it
+ *                 receives the absolute row index of the extreme (lowest
+ *                 row on ties), -1 for an empty segment.  It must be NULL
+ *                 for SEG_SUM / SEG_MEAN (SEG_ERR_INVALID_ARGUMENT otherwise).
+ *   stream        CUDA stream the work is ordered on.
+ *
+ * Returns SEG_OK when the work was enqueued.
+ */
+seg_status_t seg_reduce(const void *values, seg_dtype_t dtype, int64_t F,
+                        int64_t num_values, const void *offsets,
+                        seg_offset_dtype_t offsets_dtype,
+                        int64_t num_segments, seg_op_t op, void *out,
+                        int64_t *out_arg, seg_stream_t stream);
+
+/* Static, human-readable text for a status code (never NULL). */
+const char *seg_reduce_strerror(seg_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of
+ * the current device.  Returns SEG_OK if no call on this device has
+ * recorded a device-side error since the last read, SEG_ERR_DEVICE_TIMEOUT
+ * if a bounded wait inside a kernel ran out (that call's outputs are then
+ * incomplete), or SEG_ERR_CUDA if synchronising failed.
+ */
+seg_status_t seg_reduce_device_status(seg_stream_t stream);
+
+/*
+ * The launch the library would make, computed on the host only (no CUDA
+ * call, no device memory touched), so that it can be inspected and tested
+ * without a GPU.  `values_addr` is the address `values` would have (only
+ * its alignment matters) and `sm_count` the device's multiprocessor count.
+ */
+typedef struct {
+    int32_t grid;            /* CTAs launched (at most one per SM)                    */
+    int32_t block;           /* threads per CTA: consumer warps + one producer warp   */
+    int32_t slot_threads;    /* threads that share one row (G)                        */
+    int32_t items_per_slot;  /* merge items (rows + segment ends) per slot per tile   */
+    int32_t vec;             /* elements per shared-memory load (1 or 4)              */
+    int32_t vecs_per_thread; /* load groups per thread per row                        */
+    int32_t max_ends;        /* cap on segment ends in one tile                       */
+    int32_t kernel_variant;  /* index of the compiled kernel shape                    */
+    int64_t smem_bytes;      /* dynamic shared memory per CTA                         */
+    int64_t workspace_bytes; /* library-owned scratch the launch uses                 */
+} seg_plan_t;
+
+seg_status_t seg_reduce_plan(seg_dtype_t dtype, int64_t F, int64_t num_values,
+                             seg_offset_dtype_t offsets_dtype,
+                             int64_t num_segments, seg_op_t op,
+                             uint64_t values_addr, int32_t sm_count,
+                             seg_plan_t *plan);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t seg_reduce_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SEG_REDUCE_H */

@@ -1,0 +1,213 @@
+"""segmented_reduction_csr_gb300 -- segmented reduction over offset-delimited
+(CSR indptr) segments on NVIDIA GB300 (sm_103a).
+
+A thin ctypes binding of ``libsegreduce.so`` (C ABI in ``include/seg_reduce.h``).
+Every step of the reduction runs in the library's CUDA kernels; this module
+only checks shapes, allocates outputs with torch and passes raw pointers and
+the current CUDA stream.  There is no CPU fallback: if the library is
+missing or no GPU is present, the calls raise.
+
+Semantics (GPUSegmentedReduction "Contract"; graph-reduce README "API"):
+segment ``s`` reduces rows ``[indptr[s], indptr[s+1])`` of ``src`` (``[N]`` or
+``[N, F]``, over dimension 0); ``sum`` / ``min`` / ``max`` for uint32, int32
+and float32, ``mean`` for float32; ``min`` / ``max`` also return the absolute
+source row (int64; ties to the lower row; -1 for an empty segment); empty
+segments give 0.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "seg_reduce", "segment_sum_csr", "segment_mean_csr", "segment_min_csr",
+    "segment_max_csr", "plan", "device_status", "library_path", "load_library",
+    "SegReduceError",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "lib", "libsegreduce.so")
+
+# Codes of include/seg_reduce.h
+SEG_U32, SEG_S32, SEG_F32 = 0, 1, 2
+SEG_OFF_U32, SEG_OFF_I64 = 0, 1
+OPS = {"sum": 0, "min": 1, "max": 2, "mean": 3}
+STATUS = {0: "SEG_OK", 1: "SEG_ERR_INVALID_ARGUMENT", 2: "SEG_ERR_UNSUPPORTED",
+          3: "SEG_ERR_OUT_OF_MEMORY", 4: "SEG_ERR_CUDA", 5: "SEG_ERR_DEVICE_TIMEOUT"}
+EXPORTED = ("seg_reduce", "seg_reduce_strerror", "seg_reduce_device_status",
+            "seg_reduce_plan", "seg_reduce_version")
+
+
+class SegReduceError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({_strerror(status)})")
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [("grid", ctypes.c_int32), ("block", ctypes.c_int32),
+                ("slot_threads", ctypes.c_int32), ("items_per_slot", ctypes.c_int32),
+                ("vec", ctypes.c_int32), ("vecs_per_thread", ctypes.c_int32),
+                ("max_ends", ctypes.c_int32), ("kernel_variant", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load libsegreduce.so (raises OSError if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _LIB_PATH
+        if not os.path.exists(p):
+            raise OSError(f"{p} is missing: build it with "
+                          "`python -m segmented_reduction_csr_gb300.build`")
+        lib = ctypes.CDLL(p)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+        lib.seg_reduce.restype = ctypes.c_int
+        lib.seg_reduce.argtypes = [vp, ctypes.c_int, i64, i64, vp, ctypes.c_int, i64,
+                                   ctypes.c_int, vp, vp, vp]
+        lib.seg_reduce_strerror.restype = ctypes.c_char_p
+        lib.seg_reduce_strerror.argtypes = [ctypes.c_int]
+        lib.seg_reduce_device_status.restype = ctypes.c_int
+        lib.seg_reduce_device_status.argtypes = [vp]
+        lib.seg_reduce_plan.restype = ctypes.c_int
+        lib.seg_reduce_plan.argtypes = [ctypes.c_int, i64, i64, ctypes.c_int, i64, ctypes.c_int,
+                                        ctypes.c_uint64, i32, ctypes.POINTER(_Plan)]
+        lib.seg_reduce_version.restype = i32
+        lib.seg_reduce_version.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _strerror(status: int) -> str:
+    try:
+        return load_library().seg_reduce_strerror(status).decode()
+    except OSError:
+        return "library not loaded"
+
+
+def plan(dtype: str, feat: int, num_values: int, offsets_dtype: str, num_segments: int,
+         op: str, values_addr: int = 0, sm_count: int = 152) -> dict:
+    """The launch the library would make (host-only; no GPU needed)."""
+    pl = _Plan()
+    rc = load_library().seg_reduce_plan(
+        {"u32": SEG_U32, "s32": SEG_S32, "f32": SEG_F32}[dtype], feat, num_values,
+        {"u32": SEG_OFF_U32, "i64": SEG_OFF_I64}[offsets_dtype], num_segments, OPS[op],
+        values_addr, sm_count, ctypes.byref(pl))
+    if rc != 0:
+        raise SegReduceError(rc, "seg_reduce_plan")
+    return {f: getattr(pl, f) for f, _ in _Plan._fields_}
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _value_code(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return SEG_F32
+    if t.dtype == torch.int32:
+        return SEG_S32
+    if t.dtype == getattr(torch, "uint32", None):
+        return SEG_U32
+    raise TypeError(f"values must be float32, int32 or uint32, not {t.dtype}")
+
+
+def _offset_code(t):
+    torch = _torch()
+    if t.dtype == torch.int64:
+        return SEG_OFF_I64
+    if t.dtype == getattr(torch, "uint32", None):
+        return SEG_OFF_U32
+    raise TypeError(f"offsets must be int64 or uint32, not {t.dtype}")
+
+
+def seg_reduce(values, offsets, op: str = "sum", out=None, out_arg=None, with_arg: bool = True,
+               stream=None):
+    """Reduce ``values`` ([N] or [N, F], CUDA) over the segments that ``offsets``
+    ([S+1], CUDA, int64 or uint32) delimits.
+
+    Returns ``out`` for sum / mean, ``(out, arg)`` for min / max when
+    ``with_arg`` (arg int64, -1 for empty segments).  ``out`` / ``out_arg`` may
+    be passed preallocated.  Work is enqueued on ``stream`` (default: the
+    current stream of the values' device) and is not synchronised.
+    """
+    torch = _torch()
+    if op not in OPS:
+        raise ValueError(f"op must be one of {sorted(OPS)}")
+    if not values.is_cuda or not offsets.is_cuda:
+        raise ValueError("values and offsets must be CUDA tensors (there is no CPU path)")
+    if values.device != offsets.device:
+        raise ValueError("values and offsets must be on the same device")
+    if values.dim() not in (1, 2) or offsets.dim() != 1 or offsets.numel() < 1:
+        raise ValueError("values must be [N] or [N, F] and offsets [S+1]")
+    if not values.is_contiguous() or not offsets.is_contiguous():
+        raise ValueError("values and offsets must be contiguous")
+    lib = load_library()
+    n = values.shape[0]
+    feat = 1 if values.dim() == 1 else values.shape[1]
+    s = offsets.numel() - 1
+    oshape = (s,) if values.dim() == 1 else (s, feat)
+    if out is None:
+        out = torch.empty(oshape, dtype=values.dtype, device=values.device)
+    elif tuple(out.shape) != oshape or out.dtype != values.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous {values.dtype} tensor of shape {oshape}")
+    want_arg = op in ("min", "max") and (with_arg or out_arg is not None)
+    if want_arg and out_arg is None:
+        out_arg = torch.empty(oshape, dtype=torch.int64, device=values.device)
+    if out_arg is not None and (tuple(out_arg.shape) != oshape or out_arg.dtype != torch.int64
+                                or not out_arg.is_contiguous()):
+        raise ValueError(f"out_arg must be a contiguous int64 tensor of shape {oshape}")
+    if stream is None:
+        stream = torch.cuda.current_stream(values.device)
+    with torch.cuda.device(values.device):
+        rc = lib.seg_reduce(values.data_ptr() if n else None, _value_code(values), feat, n,
+                            offsets.data_ptr(), _offset_code(offsets), s, OPS[op],
+                            out.data_ptr() if s else None,
+                            out_arg.data_ptr() if (want_arg and s) else None,
+                            ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SegReduceError(rc, "seg_reduce")
+    return (out, out_arg) if want_arg else out
+
+
+def segment_sum_csr(src, indptr):
+    """Per-segment sum of ``src`` rows (graph-reduce README, ``segment_sum_csr``)."""
+    return seg_reduce(src, indptr, "sum")
+
+
+def segment_mean_csr(src, indptr):
+    """Per-segment mean; an empty segment gives 0."""
+    return seg_reduce(src, indptr, "mean")
+
+
+def segment_max_csr(src, indptr):
+    """``(values, arg)``: per-segment maximum and its source row."""
+    return seg_reduce(src, indptr, "max")
+
+
+def segment_min_csr(src, indptr):
+    """``(values, arg)``: per-segment minimum and its source row."""
+    return seg_reduce(src, indptr, "min")
+
+
+def device_status(stream=None) -> int:
+    """Synchronise ``stream`` and read (and clear) the device status word:
+    0 if no kernel on the current device recorded a timed-out wait."""
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return load_library().seg_reduce_device_status(ctypes.c_void_p(stream.cuda_stream))

@@ -1,0 +1,298 @@
+// api.cu -- the C ABI of libsegreduce (declared in include/seg_reduce.h):
+// argument checks, the host launch planner, the library-owned scratch cache
+// and the kernel launch.  Nothing here reads device memory on the host.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/seg_reduce.h"
+#include "seg_pick.cuh"
+
+using namespace segred;
+
+namespace {
+
+constexpr int32_t kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int kMaxDevices = 64;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Tickets sit at the start of scratch in a region sized for the largest
+// grid the device can get (one CTA per SM), so the partials of a call never
+// overlap the ticket slots of a later call with a larger grid: a ticket slot
+// only ever holds (generation << 32) | count.
+int64_t ticket_region_bytes(int32_t sm_count) { return ceil_div(int64_t(sm_count) * 8, 256) * 256; }
+
+int32_t next_pow2(int32_t x) {
+    int32_t p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+// ---------------------------------------------------------------------------
+// Planner (host only).
+
+seg_status_t plan_launch(seg_dtype_t dtype, int64_t F, int64_t num_values,
+                         seg_offset_dtype_t offsets_dtype, int64_t S, seg_op_t op,
+                         uint64_t values_addr, int32_t sm_count, seg_plan_t* pl) {
+    if (!pl) return SEG_ERR_INVALID_ARGUMENT;
+    if (dtype != SEG_U32 && dtype != SEG_S32 && dtype != SEG_F32) return SEG_ERR_INVALID_ARGUMENT;
+    if (offsets_dtype != SEG_OFF_U32 && offsets_dtype != SEG_OFF_I64) return SEG_ERR_INVALID_ARGUMENT;
+    if (op != SEG_SUM && op != SEG_MIN && op != SEG_MAX && op != SEG_MEAN) return SEG_ERR_INVALID_ARGUMENT;
+    if (F < 1 || num_values < 0 || S < 0 || sm_count < 1) return SEG_ERR_INVALID_ARGUMENT;
+    if (op == SEG_MEAN && dtype != SEG_F32) return SEG_ERR_UNSUPPORTED;
+    if (F > SEG_MAX_FEATURES) return SEG_ERR_UNSUPPORTED;
+    if (offsets_dtype == SEG_OFF_U32 && num_values > int64_t(UINT32_MAX)) return SEG_ERR_INVALID_ARGUMENT;
+
+    std::memset(pl, 0, sizeof(*pl));
+    const int64_t items = num_values + S;
+    if (F == 1) {
+        // the scalar kernel
+        const int64_t T = SC_TILE_ITEMS;
+        const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(sm_count, ceil_div(items, T)));
+        if (ceil_div(items, grid) + T >= int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;
+        pl->grid = static_cast<int32_t>(grid);
+        pl->block = SC_NTHREADS;
+        pl->slot_threads = 1;
+        pl->items_per_slot = SC_KR;
+        pl->vec = 1;
+        pl->vecs_per_thread = 1;
+        pl->max_ends = scalar_max_ends(offsets_dtype == SEG_OFF_U32 ? 4 : 8);
+        pl->kernel_variant = SHAPE_SCALAR;
+        pl->smem_bytes = op == SEG_MIN || op == SEG_MAX ? ScalarSmem<OP_MIN>::total : ScalarSmem<OP_SUM>::total;
+        pl->workspace_bytes = ticket_region_bytes(sm_count) + 2 * grid * int64_t(sizeof(PartElem));
+        return SEG_OK;
+    }
+    const int64_t esz = F * 4;
+    int32_t shape, vec, nv, G;
+    if (F % 4 == 0 && values_addr % 16 == 0) {
+        const int32_t groups = static_cast<int32_t>(F / 4);
+        nv = groups <= NT ? 1 : 2;
+        shape = nv == 1 ? SHAPE_VEC4_NV1 : SHAPE_VEC4_NV2;
+        vec = 4;
+        G = std::min<int32_t>(NT, next_pow2(static_cast<int32_t>(ceil_div(groups, nv))));
+    } else {
+        nv = F <= NT ? 1 : 8;
+        shape = nv == 1 ? SHAPE_VEC1_NV1 : SHAPE_VEC1_NV8;
+        vec = 1;
+        G = std::min<int32_t>(NT, next_pow2(static_cast<int32_t>(ceil_div(F, nv))));
+    }
+    const int32_t nslots = NT / G;
+    const int64_t budget = int64_t(VRING) - 2 * int64_t(VCHUNK);
+    const int32_t K = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(32, budget / (nslots * esz))));
+    const int64_t T = int64_t(nslots) * K;
+    const int32_t max_ends = static_cast<int32_t>(std::min<int64_t>(1024, T));
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(sm_count, ceil_div(items, T)));
+    // Rows of one CTA are addressed with 32-bit offsets inside the CTA.
+    if (ceil_div(items, grid) + T >= int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;
+
+    pl->grid = static_cast<int32_t>(grid);
+    pl->block = NTHREADS;
+    pl->slot_threads = G;
+    pl->items_per_slot = K;
+    pl->vec = vec;
+    pl->vecs_per_thread = nv;
+    pl->max_ends = max_ends;
+    pl->kernel_variant = shape;
+    pl->smem_bytes = SmemLayout::total(vec * nv);
+    pl->workspace_bytes = ticket_region_bytes(sm_count) + 2 * grid * F * int64_t(sizeof(PartElem));
+    return SEG_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Per-device state: SM count, status word, kernels already configured.
+
+struct DeviceState {
+    bool init = false;
+    int sm_count = 0;
+    unsigned int* status = nullptr;
+    std::map<const void*, bool> configured;
+};
+
+struct Scratch {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+    uint32_t gen = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
+
+seg_status_t device_state(int dev, DeviceState** out) {
+    if (dev < 0 || dev >= kMaxDevices) return SEG_ERR_CUDA;
+    DeviceState& ds = g_dev[dev];
+    if (!ds.init) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SEG_ERR_CUDA;
+        unsigned int* st = nullptr;
+        if (cudaMalloc(&st, sizeof(unsigned int)) != cudaSuccess) {
+            cudaGetLastError();
+            return SEG_ERR_OUT_OF_MEMORY;
+        }
+        if (cudaMemset(st, 0, sizeof(unsigned int)) != cudaSuccess) return SEG_ERR_CUDA;
+        ds.sm_count = sms;
+        ds.status = st;
+        ds.init = true;
+    }
+    *out = &ds;
+    return SEG_OK;
+}
+
+// Scratch for (device, stream): grown on demand, zeroed when (re)allocated,
+// stream-ordered so earlier work on the stream still sees the old buffer.
+seg_status_t scratch_for(int dev, cudaStream_t stream, size_t bytes, Scratch** out) {
+    Scratch& sc = g_scratch[std::make_pair(dev, stream)];
+    if (sc.bytes < bytes || sc.gen == UINT32_MAX) {
+        size_t want = std::max<size_t>(bytes, size_t(1) << 20);
+        want = std::max(want, sc.bytes);
+        if (sc.ptr) cudaFreeAsync(sc.ptr, stream);
+        sc.ptr = nullptr;
+        sc.bytes = 0;
+        if (cudaMallocAsync(&sc.ptr, want, stream) != cudaSuccess) {
+            cudaGetLastError();
+            sc.ptr = nullptr;
+            return SEG_ERR_OUT_OF_MEMORY;
+        }
+        if (cudaMemsetAsync(sc.ptr, 0, want, stream) != cudaSuccess) return SEG_ERR_CUDA;
+        sc.bytes = want;
+        sc.gen = 0;
+    }
+    *out = &sc;
+    return SEG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+seg_status_t seg_reduce_plan(seg_dtype_t dtype, int64_t F, int64_t num_values,
+                             seg_offset_dtype_t offsets_dtype, int64_t num_segments, seg_op_t op,
+                             uint64_t values_addr, int32_t sm_count, seg_plan_t* plan) {
+    return plan_launch(dtype, F, num_values, offsets_dtype, num_segments, op, values_addr,
+                       sm_count, plan);
+}
+
+seg_status_t seg_reduce(const void* values, seg_dtype_t dtype, int64_t F, int64_t num_values,
+                        const void* offsets, seg_offset_dtype_t offsets_dtype,
+                        int64_t num_segments, seg_op_t op, void* out, int64_t* out_arg,
+                        seg_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const int64_t S = num_segments;
+    // Host-visible argument checks; nothing is launched when one fails.
+    if (dtype != SEG_U32 && dtype != SEG_S32 && dtype != SEG_F32) return SEG_ERR_INVALID_ARGUMENT;
+    if (offsets_dtype != SEG_OFF_U32 && offsets_dtype != SEG_OFF_I64) return SEG_ERR_INVALID_ARGUMENT;
+    if (op != SEG_SUM && op != SEG_MIN && op != SEG_MAX && op != SEG_MEAN) return SEG_ERR_INVALID_ARGUMENT;
+    if (F < 1 || num_values < 0 || S < 0) return SEG_ERR_INVALID_ARGUMENT;
+    if (op == SEG_MEAN && dtype != SEG_F32) return SEG_ERR_UNSUPPORTED;
+    if (F > SEG_MAX_FEATURES) return SEG_ERR_UNSUPPORTED;
+    if ((op == SEG_SUM || op == SEG_MEAN) && out_arg != nullptr) return SEG_ERR_INVALID_ARGUMENT;
+    if (S == 0) return SEG_OK;
+    if (!offsets || !out || (num_values > 0 && !values)) return SEG_ERR_INVALID_ARGUMENT;
+    const size_t osz = offsets_dtype == SEG_OFF_U32 ? 4 : 8;
+    if (reinterpret_cast<uintptr_t>(values) % 4 || reinterpret_cast<uintptr_t>(out) % 4 ||
+        reinterpret_cast<uintptr_t>(offsets) % osz || reinterpret_cast<uintptr_t>(out_arg) % 8)
+        return SEG_ERR_INVALID_ARGUMENT;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SEG_ERR_CUDA;
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* ds = nullptr;
+    seg_status_t st = device_state(dev, &ds);
+    if (st != SEG_OK) return st;
+
+    seg_plan_t pl;
+    st = plan_launch(dtype, F, num_values, offsets_dtype, S, op,
+                     reinterpret_cast<uint64_t>(values), ds->sm_count, &pl);
+    if (st != SEG_OK) return st;
+
+    const int kop = op == SEG_MIN ? OP_MIN : (op == SEG_MAX ? OP_MAX : OP_SUM);
+    const int i64 = offsets_dtype == SEG_OFF_I64 ? 1 : 0;
+    const void* fn = dtype == SEG_U32   ? pick_kernel_u32(kop, i64, pl.kernel_variant)
+                     : dtype == SEG_S32 ? pick_kernel_s32(kop, i64, pl.kernel_variant)
+                                        : pick_kernel_f32(kop, i64, pl.kernel_variant);
+    if (!fn) return SEG_ERR_UNSUPPORTED;
+    if (!ds->configured[fn]) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(pl.smem_bytes)) != cudaSuccess) {
+            cudaGetLastError();
+            return SEG_ERR_CUDA;
+        }
+        ds->configured[fn] = true;
+    }
+
+    Scratch* sc = nullptr;
+    st = scratch_for(dev, stream, static_cast<size_t>(pl.workspace_bytes), &sc);
+    if (st != SEG_OK) return st;
+    sc->gen += 1;
+
+    Params prm;
+    prm.values = values;
+    prm.offsets = offsets;
+    prm.out = out;
+    prm.out_arg = (op == SEG_MIN || op == SEG_MAX) ? out_arg : nullptr;
+    prm.N = num_values;
+    prm.S = S;
+    prm.F = static_cast<int32_t>(F);
+    prm.G = pl.slot_threads;
+    prm.K = pl.items_per_slot;
+    prm.max_ends = pl.max_ends;
+    prm.P = pl.grid;
+    prm.mean = op == SEG_MEAN ? 1 : 0;
+    const int64_t ticket_bytes = ticket_region_bytes(ds->sm_count);
+    prm.ws_tickets = static_cast<unsigned long long*>(sc->ptr);
+    prm.ws_parts = static_cast<unsigned char*>(sc->ptr) + ticket_bytes;
+    prm.status = ds->status;
+    prm.gen = sc->gen;
+
+    void* args[] = {&prm};
+    const cudaError_t e = cudaLaunchKernel(fn, dim3(pl.grid), dim3(pl.block), args,
+                                           static_cast<size_t>(pl.smem_bytes), stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SEG_ERR_CUDA;
+    }
+    return SEG_OK;
+}
+
+const char* seg_reduce_strerror(seg_status_t status) {
+    switch (status) {
+        case SEG_OK: return "success";
+        case SEG_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case SEG_ERR_UNSUPPORTED: return "unsupported combination of arguments";
+        case SEG_ERR_OUT_OF_MEMORY: return "out of device memory for scratch";
+        case SEG_ERR_CUDA: return "CUDA runtime error";
+        case SEG_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
+        default: return "unknown status";
+    }
+}
+
+seg_status_t seg_reduce_device_status(seg_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return SEG_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SEG_ERR_CUDA;
+    unsigned int* word = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState* ds = nullptr;
+        seg_status_t st = device_state(dev, &ds);
+        if (st != SEG_OK) return st;
+        word = ds->status;
+    }
+    unsigned int h = 0;
+    if (cudaMemcpy(&h, word, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SEG_ERR_CUDA;
+    if (h != 0 && cudaMemset(word, 0, sizeof(h)) != cudaSuccess) return SEG_ERR_CUDA;
+    return h ? SEG_ERR_DEVICE_TIMEOUT : SEG_OK;
+}
+
+int32_t seg_reduce_version(void) { return kVersion; }
+
+}  // extern "C"

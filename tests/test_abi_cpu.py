@@ -1,0 +1,120 @@
+"""libsegreduce without a GPU: it loads, exports every function include/*.h
+declares, plans launches on the host, and rejects bad arguments before any
+CUDA call."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import segmented_reduction_csr_gb300 as sr
+from segmented_reduction_csr_gb300 import build as srbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    srbuild.build()
+    return sr.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(seg_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    assert {"seg_reduce", "seg_reduce_strerror", "seg_reduce_device_status",
+            "seg_reduce_plan", "seg_reduce_version"} <= set(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared but not exported"
+
+
+def test_version_and_strerror(lib):
+    assert lib.seg_reduce_version() >= 10000
+    for code in range(6):
+        assert lib.seg_reduce_strerror(code)
+    assert lib.seg_reduce_strerror(99) == b"unknown status"
+
+
+def _call(lib, values=8, dtype=2, F=1, n=10, offsets=8, odt=1, S=3, op=0, out=8, arg=None):
+    return lib.seg_reduce(values, dtype, F, n, offsets, odt, S, op, out, arg, None)
+
+
+def test_host_checks_reject_before_any_cuda_call(lib):
+    # Fake (aligned, non-null) pointers: every case returns before touching CUDA.
+    assert _call(lib, dtype=7) == 1                      # bad dtype
+    assert _call(lib, odt=5) == 1                        # bad offsets dtype
+    assert _call(lib, op=9) == 1                         # bad op
+    assert _call(lib, F=0) == 1                          # F < 1
+    assert _call(lib, n=-1) == 1                         # negative N
+    assert _call(lib, S=-1) == 1                         # negative S
+    assert _call(lib, dtype=0, op=3) == 2                # mean on uint32
+    assert _call(lib, dtype=1, op=3) == 2                # mean on int32
+    assert _call(lib, F=4096) == 2                       # F above the maximum
+    assert _call(lib, op=0, arg=8) == 1                  # sum with an arg buffer
+    assert _call(lib, op=3, arg=8) == 1                  # mean with an arg buffer
+    assert _call(lib, S=0, offsets=None, out=None) == 0  # nothing to do: no launch
+    assert _call(lib, offsets=None) == 1                 # null offsets
+    assert _call(lib, out=None) == 1                     # null out
+    assert _call(lib, values=None) == 1                  # null values with N > 0
+    assert _call(lib, values=6) == 1                     # misaligned values
+    assert _call(lib, offsets=12) == 1                   # misaligned int64 offsets
+    assert _call(lib, out=2) == 1                        # misaligned out
+    assert _call(lib, op=1, arg=4) == 1                  # misaligned arg
+
+
+def test_plan_shapes(lib):
+    p = sr.plan("f32", 1, 16_000_000, "i64", 1_000_000, "sum", sm_count=152)
+    assert p["grid"] == 152 and p["slot_threads"] == 1 and p["vec"] == 1
+    assert p["block"] == 288 and p["kernel_variant"] == 4          # the scalar kernel
+    assert p["smem_bytes"] <= 227 * 1024
+    p_u32 = sr.plan("f32", 1, 16_000, "u32", 1_000, "max", sm_count=152)
+    assert p_u32["max_ends"] > p["max_ends"] and p_u32["smem_bytes"] > p["smem_bytes"]
+    p = sr.plan("f32", 64, 1_000_000, "i64", 10_000, "max", values_addr=256, sm_count=152)
+    assert p["vec"] == 4 and p["slot_threads"] == 16 and p["vecs_per_thread"] == 1
+    p = sr.plan("f32", 64, 1_000_000, "i64", 10_000, "max", values_addr=260, sm_count=152)
+    assert p["vec"] == 1                                 # misaligned rows: scalar path
+    p = sr.plan("f32", 2048, 1000, "i64", 10, "sum", values_addr=256, sm_count=152)
+    assert p["vecs_per_thread"] == 2 and p["slot_threads"] == 256
+    p = sr.plan("f32", 130, 1000, "i64", 10, "sum", values_addr=256, sm_count=152)
+    assert p["vec"] == 1 and p["slot_threads"] == 256
+    p = sr.plan("u32", 1, 100, "u32", 10, "min", sm_count=152)
+    assert p["grid"] == 1                                # tiny input: one CTA
+    for F in (1, 2, 3, 5, 8, 64, 100, 128, 130, 1000, 1024, 2048):
+        for addr in (256, 260):
+            p = sr.plan("f32", F, 10_000_000, "i64", 100_000, "max", values_addr=addr)
+            T = (256 // p["slot_threads"]) * p["items_per_slot"]
+            # a tile's rows plus two partial chunks fit the 128 KiB value ring
+            assert T * F * 4 + 2 * 8192 <= 128 * 1024 or F == 1
+            assert p["smem_bytes"] <= 227 * 1024
+            assert p["slot_threads"] * p["vec"] * p["vecs_per_thread"] >= F
+            assert p["workspace_bytes"] >= 2 * p["grid"] * F * 16
+
+
+def test_plan_rejects(lib):
+    with pytest.raises(sr.SegReduceError):
+        sr.plan("s32", 1, 10, "i64", 2, "mean")
+    with pytest.raises(sr.SegReduceError):
+        sr.plan("f32", 4096, 10, "i64", 2, "sum")
+    with pytest.raises(sr.SegReduceError):
+        sr.plan("f32", 1, 2**33, "u32", 2, "sum")       # uint32 offsets cannot address N
+
+
+def test_python_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    v = torch.zeros(4)
+    off = torch.tensor([0, 4])
+    with pytest.raises(ValueError, match="CUDA"):
+        sr.seg_reduce(v, off, "sum")
