@@ -23,10 +23,13 @@ constexpr int kMaxDevices = 64;
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Tickets sit at the start of scratch in a region sized for the largest
-// grid the device can get (one CTA per SM), so the partials of a call never
-// overlap the ticket slots of a later call with a larger grid: a ticket slot
-// only ever holds (generation << 32) | count.
-int64_t ticket_region_bytes(int32_t sm_count) { return ceil_div(int64_t(sm_count) * 8, 256) * 256; }
+// number of cross-unit partial owners any launch on the device can have (one
+// CTA per SM, SW_NW units per CTA in the scalar kernel), so the partials of a
+// call never overlap the ticket slots of a later call with a larger grid: a
+// ticket slot only ever holds (generation << 32) | count.
+int64_t ticket_region_bytes(int32_t sm_count) {
+    return ceil_div(int64_t(sm_count) * SW_NW * 8, 256) * 256;
+}
 
 int32_t next_pow2(int32_t x) {
     int32_t p = 1;
@@ -52,20 +55,19 @@ seg_status_t plan_launch(seg_dtype_t dtype, int64_t F, int64_t num_values,
     std::memset(pl, 0, sizeof(*pl));
     const int64_t items = num_values + S;
     if (F == 1) {
-        // the scalar kernel
-        const int64_t T = SC_TILE_ITEMS;
-        const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(sm_count, ceil_div(items, T)));
-        if (ceil_div(items, grid) + T >= int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;
+        // the scalar kernel: SW_NW warp units per CTA, each at least two chunks of rows
+        const int64_t per_cta = int64_t(SW_NW) * SW_TROWS * 2;
+        const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(sm_count, ceil_div(items, per_cta)));
         pl->grid = static_cast<int32_t>(grid);
-        pl->block = SC_NTHREADS;
+        pl->block = SW_NTHREADS;
         pl->slot_threads = 1;
-        pl->items_per_slot = SC_KR;
+        pl->items_per_slot = SW_KR;
         pl->vec = 1;
         pl->vecs_per_thread = 1;
-        pl->max_ends = scalar_max_ends(offsets_dtype == SEG_OFF_U32 ? 4 : 8);
+        pl->max_ends = SW_EMAX;
         pl->kernel_variant = SHAPE_SCALAR;
-        pl->smem_bytes = op == SEG_MIN || op == SEG_MAX ? ScalarSmem<OP_MIN>::total : ScalarSmem<OP_SUM>::total;
-        pl->workspace_bytes = ticket_region_bytes(sm_count) + 2 * grid * int64_t(sizeof(PartElem));
+        pl->smem_bytes = SW_SMEM;
+        pl->workspace_bytes = ticket_region_bytes(sm_count) + 2 * grid * SW_NW * int64_t(sizeof(PartElem));
         return SEG_OK;
     }
     const int64_t esz = F * 4;

@@ -148,6 +148,30 @@ struct Carry<float, OP_SUM> {
     }
 };
 
+// The scalar kernel's float-sum carry: a compensated pair (hi + lo) kept
+// with TwoSum (Knuth), so a long chain of tile partials stays within a few
+// units of 2^-48 of the exact sum while using only float32 arithmetic.
+struct CarryF2 {
+    float hi, lo;
+};
+__device__ __forceinline__ CarryF2 two_sum_add(const CarryF2& c, float a) {
+    const float s = c.hi + a;
+    const float bb = s - c.hi;
+    const float err = (c.hi - (s - bb)) + (a - bb);
+    return CarryF2{s, c.lo + err};
+}
+template <class T, int OP>
+struct ScalarCarry : Carry<T, OP> {};
+template <>
+struct ScalarCarry<float, OP_SUM> {
+    using C = CarryF2;
+    __device__ __forceinline__ static C ident() { return C{0.0f, 0.0f}; }
+    __device__ __forceinline__ static C from(const Acc<float>& a) { return C{a.v, 0.0f}; }
+    __device__ __forceinline__ static C then(const C& c, const Acc<float>& a) {
+        return two_sum_add(c, a.v);
+    }
+};
+
 template <class T>
 __device__ __forceinline__ uint32_t bits_of(T x) {
     return *reinterpret_cast<uint32_t*>(&x);
@@ -183,6 +207,16 @@ __device__ __forceinline__ PartElem to_part(const Acc<T>& a, int64_t row_base) {
     PartElem p;
     p.v.u = bits_of(a.v);
     p.row = (OP != OP_SUM && a.row >= 0) ? row_base + a.row : -1;
+    return p;
+}
+__device__ __forceinline__ void finish_carry(const CarryF2& c, int64_t len, int mean, float& v) {
+    const float s = c.hi + c.lo;
+    v = mean ? (len > 0 ? s / static_cast<float>(len) : 0.0f) : s;
+}
+__device__ __forceinline__ PartElem to_part(const CarryF2& c) {
+    PartElem p;
+    p.v.d = static_cast<double>(c.hi) + static_cast<double>(c.lo);
+    p.row = -1;
     return p;
 }
 __device__ __forceinline__ PartElem to_part(const CarryD& c) {
@@ -251,13 +285,11 @@ __device__ __forceinline__ Stream make_stream(uint64_t buf, uint64_t buf_bytes, 
     return s;
 }
 
-// Producer side: put chunk m of stream `s` into its ring stage.
-__device__ __forceinline__ void issue_chunk(const Stream& s, int64_t m, unsigned char* ring,
-                                            uint32_t ring_bytes, uint32_t chunk, uint64_t* full,
-                                            uint64_t policy) {
+// Producer side: copy chunk m of stream `s` (chunk bytes from A0) to `dst`.
+__device__ __forceinline__ void issue_chunk_to(const Stream& s, int64_t m, uint32_t chunk,
+                                               unsigned char* dst, uint64_t* full, uint64_t policy) {
     const uint64_t cs = s.A0 + static_cast<uint64_t>(m) * chunk;
     const uint64_t ce = cs + chunk < s.AE ? cs + chunk : s.AE;
-    unsigned char* dst = ring + ((cs - s.A0) & (ring_bytes - 1));
     const uint64_t ts = cs > s.TA ? cs : s.TA;
     const uint64_t te = ce < s.TE ? ce : s.TE;
     const uint32_t tx = te > ts ? static_cast<uint32_t>(te - ts) : 0u;
@@ -275,6 +307,14 @@ __device__ __forceinline__ void issue_chunk(const Stream& s, int64_t m, unsigned
     }
     mbar_arrive_expect_tx(full, tx);
     if (tx) bulk_load(dst + (ts - cs), reinterpret_cast<const void*>(ts), tx, full, policy);
+}
+
+// Same, into a power-of-two ring: byte A0 + k lands at ring offset k mod ring_bytes.
+__device__ __forceinline__ void issue_chunk(const Stream& s, int64_t m, unsigned char* ring,
+                                            uint32_t ring_bytes, uint32_t chunk, uint64_t* full,
+                                            uint64_t policy) {
+    const uint64_t cs = s.A0 + static_cast<uint64_t>(m) * chunk;
+    issue_chunk_to(s, m, chunk, ring + ((cs - s.A0) & (ring_bytes - 1)), full, policy);
 }
 
 // Wait for a phase with a time limit; records `code` in the status word on expiry.

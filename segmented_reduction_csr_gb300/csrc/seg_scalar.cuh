@@ -1,457 +1,610 @@
 // seg_scalar.cuh -- the scalar kernel: F == 1 vectors of uint32, int32 or
 // float32 (GPUSegmentedReduction's "packed scalar values").
 //
-// Each CTA walks its merge range in tiles of up to SC_ROWS rows.  A tile is
-// processed in three branch-free passes so that every row costs a couple of
-// instructions whatever the segment lengths:
+// Work split.  The merge path of rows and segment ends is cut into units of
+// equal length, one unit per warp (SW_NW warps per CTA, one CTA per SM).  A
+// CTA finds the SW_NW + 1 unit boundaries it needs with one cooperative
+// search; after that every warp runs on its own: no CTA barrier in the main
+// loop, so the latency of one warp's steps hides behind the others.
 //
-//  1. Segment pass (threads stride over the tile's segment ends): mark in
-//     `keep` (one 32-bit mask per row) every row where a segment starts.
-//  2. Row pass: thread t owns SC_KR consecutive rows of a 16-byte-aligned
-//     block; it loads them with 128-bit shared loads (SC_KR / 4 is odd, so
-//     the loads are bank-conflict free), runs an inclusive segmented scan in
-//     registers (sum: acc = (acc & keep) + x, so a reset never multiplies a
-//     NaN or an Inf; min / max: strict compare, restart at a mark) and
-//     writes the running values back over the rows.  The thread totals are
-//     combined by a segmented scan across the warp (shuffles) and then
-//     across warps in order, giving each thread the running value of the
-//     rows before its block.
-//  3. Segment pass again: the result of segment s is the running value at its
-//     last row, joined with the running value before that row's thread when
-//     the segment started in an earlier thread, and with the carry of
-//     earlier tiles when it started in an earlier tile.  Consecutive threads
-//     write consecutive segments, so the stores coalesce.  The same pass
-//     clears the marks and computes the carry for the segment left open.
+// Per warp.  Lane 0 streams the unit's rows (SW_VCHUNK-byte chunks, SW_NSV
+// stages) and offsets (a SW_NSO-stage ring) into the warp's shared memory
+// with 1-D bulk copies, refilling a stage as soon as the warp is done with it.
+// A tile is the rows of one chunk plus the segment ends that fall in them (at
+// most SW_EMAX ends; a chunk with more is split into several tiles):
 //
-// Shared memory: the value ring (rows are rewritten in place with running
-// values), the offsets ring, the row marks, the running rows of min / max.
+//  1. marks: every lane takes segment ends and sets the bit of the row where
+//     the next segment starts (a 20-bit word per lane), plus the tile's first row;
+//  2. rows: lane l owns rows [20 l, 20 l + 20) of the chunk, loads them with
+//     128-bit shared loads (the 80-byte lane stride makes them conflict free),
+//     runs an inclusive segmented scan in registers (sum: restart at a mark;
+//     min / max: strict compare, restart at a mark; rows arrive in order so
+//     ties keep the lower row) and writes the running values back;  a
+//     segmented shuffle scan over the lanes gives each lane the running value
+//     of the rows before it;
+//  3. ends: every lane takes a segment end; its result is the running value at
+//     the segment's last row, joined with the owning lane's prefix (a shuffle)
+//     when the segment started in an earlier lane, and with the warp's carry
+//     when it started in an earlier tile.  Consecutive lanes store consecutive
+//     segments.  The carry of the segment left open is taken the same way.
+//
+// A segment that crosses units leaves per-unit partials in scratch; the last
+// unit to arrive (atomic ticket, no waiting) combines them in unit order with
+// a lane-parallel tree, so float results are reproducible.
 #pragma once
 #include "seg_common.cuh"
 
 namespace segred {
 
-constexpr int SC_NT = 256;                  // consumer threads (8 warps)
-constexpr int SC_NTHREADS = SC_NT + 32;     // + one producer warp
-constexpr int SC_KR = 36;                   // rows per thread per tile (SC_KR / 4 odd)
-constexpr int SC_ROWS = SC_NT * SC_KR;      // rows a tile's blocks can hold
-constexpr int64_t SC_TILE_ITEMS = SC_ROWS - 3;  // merge items per tile (block alignment slack)
-constexpr uint32_t SC_VRING = 128u * 1024u;
-constexpr uint32_t SC_VCHUNK = 8u * 1024u;
-constexpr int SC_NSV = SC_VRING / SC_VCHUNK;
-constexpr uint32_t SC_ORING = 16u * 1024u;
-constexpr uint32_t SC_OCHUNK = 1024u;
-constexpr int SC_NSO = SC_ORING / SC_OCHUNK;
-static_assert((SC_KR / 4) % 2 == 1, "conflict-free 128-bit row loads need SC_KR / 4 odd");
-// Ring stages are handed back one tile late, so each ring holds two tiles.
-static_assert(2 * SC_ROWS * 4 + 2 * SC_VCHUNK <= SC_VRING, "value ring too small for two tiles");
+constexpr int SW_NW = 16;                      // warps (units) per CTA
+constexpr int SW_NTHREADS = SW_NW * 32;
+constexpr int SW_KR = 20;                      // rows per lane per tile (SW_KR / 4 odd)
+constexpr int SW_TROWS = 32 * SW_KR;           // rows per value chunk
+constexpr uint32_t SW_VCHUNK = SW_TROWS * 4;   // bytes per value chunk
+constexpr int SW_NSV = 3;                      // value stages per warp
+constexpr uint32_t SW_OCHUNK = 512;            // bytes per offsets chunk
+constexpr int SW_NSO = 4;                      // offsets stages per warp
+constexpr uint32_t SW_ORING = SW_OCHUNK * SW_NSO;
+constexpr int SW_EMAX = 64;                    // segment ends per tile (two per lane)
+constexpr int SW_NDIAG = SW_NW + 1;            // unit boundaries per CTA
+constexpr int SW_GRID = 1024;                  // first-round probes, shared by all CTAs
+constexpr int SW_PROBES = 60;                  // later-round probes per boundary
+static_assert((SW_KR / 4) % 2 == 1, "conflict-free 128-bit row loads need SW_KR / 4 odd");
+static_assert(SW_NDIAG * SW_PROBES <= 2 * SW_NTHREADS, "two probes per thread per round");
+static_assert((SW_EMAX + 1) * 8 + SW_OCHUNK <= SW_ORING, "offsets ring holds a tile's window");
+static_assert(SW_EMAX == 64, "each lane holds two of a tile's segment ends");
 
-// Largest number of segment ends one tile may hold: two windows of
-// (max_ends + 1) offsets plus two partial chunks fit the offsets ring.
-__host__ __device__ constexpr int scalar_max_ends(int offset_bytes) {
-    return static_cast<int>((SC_ORING - 2 * SC_OCHUNK) / (2u * offset_bytes)) - 2;
+// Per-warp shared memory.
+struct WarpSmem {
+    static constexpr uint32_t vstage = 0;
+    static constexpr uint32_t oring = SW_NSV * SW_VCHUNK;
+    static constexpr uint32_t marks = oring + SW_ORING;
+    static constexpr uint32_t argr = marks + 32 * 4;
+    static constexpr uint32_t bars = argr + SW_TROWS * 2;
+    static constexpr uint32_t bytes = ((bars + (SW_NSV + SW_NSO) * 8 + 1023) / 1024) * 1024;
+};
+constexpr uint32_t SW_SMEM = SW_NW * WarpSmem::bytes;
+
+// Search scratch (aliases the warps' memory before they start).
+struct SearchSmem {
+    int64_t graw[SW_GRID];
+    int64_t D[SW_NDIAG], lo[SW_NDIAG], hi[SW_NDIAG];
+    int cnt[SW_NDIAG];
+    int64_t o0, oS;
+};
+static_assert(sizeof(SearchSmem) <= SW_SMEM, "search scratch fits");
+
+// Last arriver of a multi-unit segment: partials tails[pc .. qc-1] then
+// heads[qc], combined by the whole warp: lane l folds a contiguous block in
+// order, then lanes fold pairwise in order (a fixed tree), lane 0 stores.
+template <class T, int OP>
+__device__ __forceinline__ void warp_combine_store(const Params& p, const PartElem* tails,
+                                                   const PartElem* heads, int pc, int qc, int64_t s,
+                                                   int64_t len, int lane) {
+    const int n = qc - pc + 1;
+    const int per = (n + 31) / 32;
+    PartElem a;
+    a.v.d = 0.0;
+    a.row = -1;
+    bool have = false;
+    for (int t = 0; t < per; ++t) {
+        const int k = pc + lane * per + t;
+        if (k <= qc) {
+            const PartElem pe = load_part(k < qc ? &tails[k] : &heads[qc]);
+            a = have ? part_comb<T, OP>(a, pe) : pe;
+            have = true;
+        }
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        PartElem b;
+        b.v.d = __longlong_as_double(__shfl_down_sync(0xffffffffu, __double_as_longlong(a.v.d), o));
+        b.row = __shfl_down_sync(0xffffffffu, a.row, o);
+        const bool bh = __shfl_down_sync(0xffffffffu, have, o);
+        if ((lane & (2 * o - 1)) == 0 && bh) {
+            a = have ? part_comb<T, OP>(a, b) : b;
+            have = true;
+        }
+    }
+    if (lane == 0) {
+        T v;
+        int64_t ar;
+        finish_part<T, OP>(a, len, p.mean, v, ar);
+        static_cast<T*>(p.out)[s] = v;
+        if (OP != OP_SUM && p.out_arg != nullptr) p.out_arg[s] = ar;
+    }
 }
 
-template <int OP>
-struct ScalarSmem {
-    static constexpr uint32_t vring = 0;
-    static constexpr uint32_t oring = SC_VRING;
-    static constexpr uint32_t keep = oring + SC_ORING;
-    static constexpr uint32_t argr = keep + SC_ROWS * 4;
-    static constexpr uint32_t argr_bytes = OP == OP_SUM ? 0 : SC_ROWS * 4;
-    static constexpr uint32_t bars = argr + argr_bytes;
-    static constexpr uint32_t misc = bars + 2 * (SC_NSV + SC_NSO) * 8;   // search counts, tile message
-    static constexpr uint32_t carry = misc + 128;                        // [2] x 16 bytes
-    static constexpr uint32_t xv = carry + 32;                           // [SC_NT] thread prefixes
-    static constexpr uint32_t xr = xv + SC_NT * 4;
-    static constexpr uint32_t wv = xr + SC_NT * 4;                       // [8] warp totals
-    static constexpr uint32_t wr = wv + 32;
-    static constexpr uint32_t wf = wr + 32;
-    static constexpr uint32_t total = wf + 32;
-};
-
-struct TileMsg {
-    int64_t d_end, i_end, j_end;
-};
-
 template <class T, int OP, class OffT>
-__global__ void __launch_bounds__(SC_NTHREADS, 1) seg_scalar_kernel(const Params p) {
+__global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params p) {
     using RD = Red<T, OP>;
     using CO = Carry<T, OP>;
     using C = typename CO::C;
-    using L = ScalarSmem<OP>;
     constexpr uint32_t OSZ = sizeof(OffT);
-    static_assert(sizeof(C) <= 16, "carry slot");
 
     extern __shared__ __align__(1024) unsigned char smem[];
-    unsigned char* vring = smem + L::vring;
-    unsigned char* oring = smem + L::oring;
-    uint32_t* keep = reinterpret_cast<uint32_t*>(smem + L::keep);
-    int32_t* argr = reinterpret_cast<int32_t*>(smem + L::argr);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
-    uint64_t* full_v = bars;
-    uint64_t* empty_v = full_v + SC_NSV;
-    uint64_t* full_o = empty_v + SC_NSV;
-    uint64_t* empty_o = full_o + SC_NSO;
-    int* counts = reinterpret_cast<int*>(smem + L::misc);
-    TileMsg* tm = reinterpret_cast<TileMsg*>(smem + L::misc + 32);
-    C* carry_buf = reinterpret_cast<C*>(smem + L::carry);
-    T* xv = reinterpret_cast<T*>(smem + L::xv);
-    int32_t* xr = reinterpret_cast<int32_t*>(smem + L::xr);
-    T* wv = reinterpret_cast<T*>(smem + L::wv);
-    int32_t* wr = reinterpret_cast<int32_t*>(smem + L::wr);
-    int* wf = reinterpret_cast<int*>(smem + L::wf);
-
     const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int cta = blockIdx.x;
     const int64_t N = p.N;
     const int64_t S = p.S;
     const OffT* offs = static_cast<const OffT*>(p.offsets);
+    const int64_t U = static_cast<int64_t>(p.P) * SW_NW;   // units in the grid
 
-    if (tid < 6) counts[tid] = 0;
-    if (tid == 0) {
-        init_ring_barriers(bars, SC_NSV, SC_NSO);
-        carry_buf[0] = CO::ident();
-    }
-    if (tid < SC_NT) {
-#pragma unroll
-        for (int q = 0; q < SC_KR / 4; ++q)
-            *reinterpret_cast<uint4*>(&keep[tid * SC_KR + 4 * q]) = make_uint4(~0u, ~0u, ~0u, ~0u);
+    // ---- a2: unit boundaries ---------------------------------------------------
+    // I(D) = #{s : key(s) < D}, key(s) = (offsets[s+1] - o0) + s.  Round 1
+    // reads a fixed grid of SW_GRID keys that every CTA shares (so it hits L2);
+    // then each boundary narrows its bracket with SW_PROBES probes per round.
+    SearchSmem* ss = reinterpret_cast<SearchSmem*>(smem);
+    if (tid == 0) ss->o0 = clamp_off(__ldg(&offs[0]), N);
+    if (tid == 1) ss->oS = clamp_off(__ldg(&offs[S]), N);
+    for (int m = tid; m < SW_GRID; m += SW_NTHREADS) {
+        const int64_t sm = static_cast<int64_t>(m) * S / SW_GRID;
+        ss->graw[m] = clamp_off(__ldg(&offs[sm + 1]), N);
     }
     __syncthreads();
-    CtaRange cr;
-    if (!cta_range<SC_NTHREADS, OffT>(p, counts, cr)) return;
-    const int64_t o0 = cr.o0, W = cr.W, Dlo = cr.Dlo, Dhi = cr.Dhi;
-    const int64_t Ilo = cr.Ilo, Ihi = cr.Ihi, Rlo = cr.Rlo, Rhi = cr.Rhi;
-    const int cta = blockIdx.x;
-
-    const uint64_t vbase = reinterpret_cast<uint64_t>(p.values);
-    const uint64_t obase = reinterpret_cast<uint64_t>(p.offsets);
-    const Stream vs = make_stream(vbase, static_cast<uint64_t>(N) * 4, vbase + Rlo * 4,
-                                  vbase + Rhi * 4, SC_VCHUNK);
-    const Stream os = make_stream(obase, static_cast<uint64_t>(S + 1) * OSZ, obase + Ilo * OSZ,
-                                  obase + (Ihi + 1) * OSZ, SC_OCHUNK);
-    if (tid >= SC_NT) {
-        if (tid == SC_NT)
-            producer_loop<SC_VRING, SC_VCHUNK, SC_ORING, SC_OCHUNK>(vs, os, vring, oring, full_v,
-                                                                    empty_v, full_o, empty_o, p.status);
-        return;
+    const int64_t o0 = ss->o0;
+    const int64_t oS = ss->oS < o0 ? o0 : ss->oS;
+    const int64_t nrows = oS - o0;
+    const int64_t total = nrows + S;
+    const int64_t Wu = (total + U - 1) / U;
+    if (tid < SW_NDIAG) {
+        const int64_t u = static_cast<int64_t>(cta) * SW_NW + tid;
+        const int64_t D = u * Wu < total ? u * Wu : total;
+        int64_t lo = D - nrows > 0 ? D - nrows : 0;
+        int64_t hi = D < S ? D : S;
+        int a = 0, b = SW_GRID;   // c = #{m : key(s_m) < D}
+        while (a < b) {
+            const int mid = (a + b) >> 1;
+            const int64_t sm = static_cast<int64_t>(mid) * S / SW_GRID;
+            if (ss->graw[mid] - o0 + sm < D)
+                a = mid + 1;
+            else
+                b = mid;
+        }
+        const int64_t lower = a > 0 ? static_cast<int64_t>(a - 1) * S / SW_GRID + 1 : 0;
+        const int64_t upper = a < SW_GRID ? static_cast<int64_t>(a) * S / SW_GRID : S;
+        lo = lo > lower ? lo : lower;
+        hi = hi < upper ? hi : upper;
+        if (hi < lo) hi = lo;
+        ss->D[tid] = D;
+        ss->lo[tid] = lo;
+        ss->hi[tid] = hi;
+        ss->cnt[tid] = 0;
     }
+    __syncthreads();
+    for (int round = 0; round < 64; ++round) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int pidx = tid + u * SW_NTHREADS;
+            const int k = pidx / SW_PROBES;
+            const int mm = pidx - k * SW_PROBES;
+            if (k < SW_NDIAG) {
+                const int64_t lo = ss->lo[k], hi = ss->hi[k];
+                const int64_t len = hi - lo;
+                if (len > 0) {
+                    const int64_t step = (len + SW_PROBES - 1) / SW_PROBES;
+                    const int64_t s = lo + mm * step;
+                    if (s < hi && clamp_off(__ldg(&offs[s + 1]), N) - o0 + s < ss->D[k])
+                        atomicAdd(&ss->cnt[k], 1);
+                }
+            }
+        }
+        __syncthreads();
+        bool open = false;
+        if (tid < SW_NDIAG) {
+            int64_t lo = ss->lo[tid], hi = ss->hi[tid];
+            const int64_t len = hi - lo;
+            if (len > 0) {
+                const int64_t step = (len + SW_PROBES - 1) / SW_PROBES;
+                const int64_t c = ss->cnt[tid];
+                if (c == 0) {
+                    hi = lo;
+                } else {
+                    const int64_t last = lo + (c - 1) * step;
+                    hi = last + step < hi ? last + step : hi;
+                    lo = last + 1 < hi ? last + 1 : hi;
+                }
+                ss->lo[tid] = lo;
+                ss->hi[tid] = hi;
+                ss->cnt[tid] = 0;
+                open = lo < hi;
+            }
+        }
+        if (!__syncthreads_or(open)) break;
+    }
+    // my unit: merge positions [D_w, D_w+1), ends [Iu, Iu2), rows [Ru, Ru2)
+    const int64_t u_me = static_cast<int64_t>(cta) * SW_NW + warp;
+    const int64_t Dlo = ss->D[warp], Dhi = ss->D[warp + 1];
+    const int64_t Iu = ss->lo[warp];
+    const int64_t Iu2 = ss->lo[warp + 1] > Iu ? ss->lo[warp + 1] : Iu;
+    int64_t Ru = Dlo - Iu + o0;
+    Ru = Ru < o0 ? o0 : (Ru > oS ? oS : Ru);
+    int64_t Ru2 = Dhi - Iu2 + o0;
+    Ru2 = Ru2 < Ru ? Ru : (Ru2 > oS ? oS : Ru2);
+    __syncthreads();   // the search scratch is dead from here on
+    if (Dlo >= Dhi) return;
 
-    // ---- consumers ------------------------------------------------------------
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
+    // ---- per-warp state ----------------------------------------------------------
+    unsigned char* wbase = smem + warp * WarpSmem::bytes;
+    unsigned char* vst = wbase + WarpSmem::vstage;
+    unsigned char* oring = wbase + WarpSmem::oring;
+    uint32_t* marks = reinterpret_cast<uint32_t*>(wbase + WarpSmem::marks);
+    int16_t* argr = reinterpret_cast<int16_t*>(wbase + WarpSmem::argr);
+    uint64_t* fv = reinterpret_cast<uint64_t*>(wbase + WarpSmem::bars);
+    uint64_t* fo = fv + SW_NSV;
     T* out = static_cast<T*>(p.out);
     PartElem* tails = static_cast<PartElem*>(p.ws_parts);
-    PartElem* heads = tails + static_cast<int64_t>(p.P);
+    PartElem* heads = tails + U;
     const int mean = p.mean;
     const bool want_arg = (OP != OP_SUM) && p.out_arg != nullptr;
 
-    auto off_r = [&](int64_t s) -> int64_t {
+    const uint64_t vbase = reinterpret_cast<uint64_t>(p.values);
+    const uint64_t obase = reinterpret_cast<uint64_t>(p.offsets);
+    const Stream vs = make_stream(vbase, static_cast<uint64_t>(N) * 4, vbase + Ru * 4, vbase + Ru2 * 4,
+                                  SW_VCHUNK);
+    const Stream os = make_stream(obase, static_cast<uint64_t>(S + 1) * OSZ, obase + Iu * OSZ,
+                                  obase + (Iu2 + 1) * OSZ, SW_OCHUNK);
+    const int64_t vrow0 = static_cast<int64_t>(vs.A0 - vbase) / 4;   // row of chunk 0's first byte
+    const uint64_t policy = policy_evict_first();
+
+    marks[lane] = 0u;
+    if (lane == 0) {
+        for (int k = 0; k < SW_NSV + SW_NSO; ++k) mbar_init(&fv[k], 1);
+        fence_mbarrier_init();
+    }
+    __syncwarp();
+    int64_t v_issued = 0, o_issued = 0;       // lane 0's counters (kept uniform by shuffles)
+    if (lane == 0) {
+        for (; v_issued < SW_NSV && v_issued < vs.nch; ++v_issued)
+            issue_chunk_to(vs, v_issued, SW_VCHUNK, vst + (v_issued % SW_NSV) * SW_VCHUNK,
+                           &fv[v_issued % SW_NSV], policy);
+        for (; o_issued < SW_NSO && o_issued < os.nch; ++o_issued)
+            issue_chunk(os, o_issued, oring, SW_ORING, SW_OCHUNK, &fo[o_issued % SW_NSO], policy);
+    }
+
+    auto off_w = [&](int64_t s) -> int64_t {
         const uint32_t at = static_cast<uint32_t>((obase + static_cast<uint64_t>(s) * OSZ) - os.A0) &
-                            (SC_ORING - 1);
+                            (SW_ORING - 1);
         return clamp_off(*reinterpret_cast<const OffT*>(oring + at), N);
     };
-    auto key_r = [&](int64_t s) -> int64_t { return off_r(s + 1) - o0 + s; };
-    auto ring_at = [&](int64_t row) -> uint32_t {
-        return static_cast<uint32_t>((vbase + static_cast<uint64_t>(row) * 4) - vs.A0) & (SC_VRING - 1);
+    int64_t ow = 0, odone = 0;   // offsets chunks waited for / handed back
+    bool ok = true;
+    // wait until offsets entry x is in the ring (uniform across the warp)
+    auto wait_offsets = [&](int64_t x) {
+        const int64_t need =
+            static_cast<int64_t>((obase + static_cast<uint64_t>(x + 1) * OSZ - 1 - os.A0) / SW_OCHUNK);
+        if (ow <= need && ow < os.nch) {
+            if (lane == 0)
+                for (; ok && ow <= need && ow < os.nch; ++ow)
+                    ok = wait_bounded(&fo[ow % SW_NSO], static_cast<uint32_t>((ow / SW_NSO) & 1), p.status,
+                                      STATUS_CONSUMER_TIMEOUT);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ow = __shfl_sync(0xffffffffu, ow, 0);
+            __syncwarp();
+        }
     };
 
-    bool head_pending = (Ilo < S) && (clamp_off(__ldg(&offs[Ilo]), N) < Rlo);
-    int64_t d = Dlo, i = Ilo, j = Rlo;
-    int64_t vw = 0, vrel = 0, ow = 0, orel = 0;
-    int par = 0;
+    C carry = CO::ident();
+    const int64_t off_Iu = clamp_off(__ldg(&offs[Iu]), N);
+    bool head_pending = (Iu < S) && off_Iu < Ru;
+    int64_t m = 0;            // current value chunk
+    bool m_ready = false;
+    int64_t es = Iu;          // next segment end
+    int64_t b_es = off_Iu;    // offsets[es]
+    int64_t j = Ru;           // next row
 
-    while (d < Dhi) {
-        // (A)-(C), warp 0: wait for the offsets window, find the tile's end,
-        // wait for its rows.
-        bool ok = true;
-        if (warp == 0) {
-            const int64_t cap_i = i + p.max_ends < Ihi ? i + p.max_ends : Ihi;
-            const int64_t need_o =
-                static_cast<int64_t>((obase + static_cast<uint64_t>(cap_i + 1) * OSZ - 1 - os.A0) / SC_OCHUNK);
-            for (; ok && ow <= need_o && ow < os.nch; ++ow)
-                ok = wait_bounded(&full_o[ow % SC_NSO], static_cast<uint32_t>((ow / SC_NSO) & 1), p.status,
+    while (ok) {
+        const bool lastc = m + 1 >= vs.nch;
+        const int64_t crow0 = vrow0 + m * SW_TROWS;
+        const int64_t rl = lastc ? Ru2 : (crow0 + SW_TROWS < Ru2 ? crow0 + SW_TROWS : Ru2);
+        if (m < vs.nch && !m_ready) {
+            if (lane == 0)
+                ok = wait_bounded(&fv[m % SW_NSV], static_cast<uint32_t>((m / SW_NSV) & 1), p.status,
                                   STATUS_CONSUMER_TIMEOUT);
-            int64_t d_end = d + SC_TILE_ITEMS < Dhi ? d + SC_TILE_ITEMS : Dhi;
-            int64_t i_end = i;
-            if (ok) {
-                if (cap_i < Ihi && key_r(cap_i - 1) < d_end) {
-                    i_end = cap_i;
-                    d_end = key_r(cap_i - 1) + 1;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();
+            m_ready = true;
+            if (!ok) break;
+        }
+        const int64_t rem = Iu2 - es;
+        const int ncand = static_cast<int>(rem < SW_EMAX ? rem : SW_EMAX);
+        wait_offsets(es + ncand);
+        if (!ok) break;
+        // Lane l holds ends es + l and es + 32 + l: E = offsets[s + 1] (the
+        // segment's end, which is the next segment's start), B = offsets[s].
+        int64_t E[2], B[2];
+        bool have[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int idx = 32 * k + lane;
+            have[k] = idx < ncand;
+            E[k] = have[k] ? off_w(es + idx + 1) : INT64_MAX;
+        }
+        {
+            const int64_t up0 = __shfl_up_sync(0xffffffffu, E[0], 1);
+            const int64_t up1 = __shfl_up_sync(0xffffffffu, E[1], 1);
+            const int64_t last0 = __shfl_sync(0xffffffffu, E[0], 31);
+            B[0] = lane == 0 ? b_es : up0;
+            B[1] = lane == 0 ? last0 : up1;
+        }
+        // ends of this tile: a prefix of those whose segment ends by row rl
+        // (all of them on the unit's last chunk)
+        int n_e = ncand;
+        if (!lastc) {
+            const unsigned b0 = __ballot_sync(0xffffffffu, have[0] && E[0] <= rl);
+            int run = b0 == 0xffffffffu ? 32 : __ffs(~b0) - 1;
+            if (run == 32) {
+                const unsigned b1 = __ballot_sync(0xffffffffu, have[1] && E[1] <= rl);
+                run += b1 == 0xffffffffu ? 32 : __ffs(~b1) - 1;
+            }
+            n_e = run < ncand ? run : ncand;
+        }
+        int64_t tr1 = rl;
+        if (n_e == SW_EMAX && es + n_e < Iu2) {
+            const int64_t x = __shfl_sync(0xffffffffu, E[1], 31);   // rows up to the last included end
+            tr1 = x < j ? j : (x > rl ? rl : x);
+        }
+        if (n_e == 0 && j >= tr1) {
+            // nothing left in this chunk
+            if (lastc) break;
+            __syncwarp();
+            if (lane == 0 && v_issued < vs.nch) {
+                issue_chunk_to(vs, v_issued, SW_VCHUNK, vst + (v_issued % SW_NSV) * SW_VCHUNK,
+                               &fv[v_issued % SW_NSV], policy);
+                ++v_issued;
+            }
+            ++m;
+            m_ready = false;
+            continue;
+        }
+
+        // ---- one tile: rows [j, tr1) of chunk m, ends [es, es + n_e) ----------------
+        unsigned char* stage = vst + (m % SW_NSV) * SW_VCHUNK;
+        const int32_t jr = static_cast<int32_t>(j - crow0);       // rows relative to the chunk
+        const int32_t tr = static_cast<int32_t>(tr1 - crow0);
+        const bool has_rows = tr1 > j && m < vs.nch;
+        const int32_t crow_u = static_cast<int32_t>(crow0 - Ru);  // chunk row 0, relative to the unit
+        Acc<T> X = RD::ident();   // running value of the rows before my lane's rows
+        if (has_rows) {
+            // 1. marks: the segment after each of this tile's ends starts at its E
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (32 * k + lane < n_e && E[k] >= j && E[k] < tr1) {
+                    const int32_t rr = static_cast<int32_t>(E[k] - crow0);
+                    atomicOr(&marks[rr / SW_KR], 1u << (rr % SW_KR));
+                }
+            }
+            if (lane == 0) atomicOr(&marks[jr / SW_KR], 1u << (jr % SW_KR));
+            __syncwarp();
+            // 2. rows
+            const uint32_t w = marks[lane];
+            marks[lane] = 0u;
+            uint32_t xb[SW_KR];
+#pragma unroll
+            for (int q = 0; q < SW_KR / 4; ++q) {
+                const uint4 u4 = *reinterpret_cast<const uint4*>(stage + lane * (SW_KR * 4) + 16 * q);
+                xb[4 * q + 0] = u4.x;
+                xb[4 * q + 1] = u4.y;
+                xb[4 * q + 2] = u4.z;
+                xb[4 * q + 3] = u4.w;
+            }
+            const int32_t lrow0 = lane * SW_KR;              // my first row, relative to the chunk
+            Acc<T> acc = RD::ident();
+            int16_t rr[OP == OP_SUM ? 1 : SW_KR];
+#pragma unroll
+            for (int k = 0; k < SW_KR; ++k) {
+                const T x = from_bits<T>(xb[k]);
+                const bool reset = (w >> k) & 1u;
+                if constexpr (OP == OP_SUM) {
+                    acc.v = reset ? x : add_wrap(acc.v, x);
                 } else {
-                    int64_t a = i, b = cap_i;
-                    while (a < b) {
-                        const int64_t mid = a + ((b - a) >> 1);
-                        if (key_r(mid) < d_end)
-                            a = mid + 1;
-                        else
-                            b = mid;
+                    const bool better = (OP == OP_MIN) ? (x < acc.v) : (x > acc.v);
+                    if (reset || acc.row < 0 || better) {
+                        acc.v = x;
+                        acc.row = crow_u + lrow0 + k;
                     }
-                    i_end = a;
+                    rr[k] = static_cast<int16_t>(acc.row - crow_u);
                 }
+                xb[k] = bits_of(acc.v);
             }
-            // Valid offsets give i <= i_end <= cap_i and d < d_end; the clamps
-            // only keep malformed offsets from stalling the loop.
-            i_end = i_end < i ? i : (i_end > cap_i ? cap_i : i_end);
-            if (d_end <= d) d_end = d + 1;
-            int64_t j_end = d_end - i_end + o0;
-            j_end = j_end < j ? j : (j_end > Rhi ? Rhi : j_end);
-            if (j_end - j > SC_TILE_ITEMS) j_end = j + SC_TILE_ITEMS;
-            if (j_end > j) {
-                const int64_t need_v =
-                    static_cast<int64_t>((vbase + static_cast<uint64_t>(j_end) * 4 - 1 - vs.A0) / SC_VCHUNK);
-                for (; ok && vw <= need_v && vw < vs.nch; ++vw)
-                    ok = wait_bounded(&full_v[vw % SC_NSV], static_cast<uint32_t>((vw / SC_NSV) & 1),
-                                      p.status, STATUS_CONSUMER_TIMEOUT);
-            }
-            if (lane == 0) {
-                tm->d_end = d_end;
-                tm->i_end = i_end;
-                tm->j_end = j_end;
-            }
-        }
-        // (D) every consumer: data is in, the previous tile is finished.
-        if (!named_bar_and<SC_NT>(ok)) return;
-        const int64_t d_end = tm->d_end, i_end = tm->i_end, j_end = tm->j_end;
-        if (tid == 0) {
-            // Stages that hold only rows before j and offsets before entry i.
-            const uint64_t vlimit = vbase + static_cast<uint64_t>(j) * 4;
-            while (vrel < vw && vs.A0 + static_cast<uint64_t>(vrel + 1) * SC_VCHUNK <= vlimit) {
-                mbar_arrive(&empty_v[vrel % SC_NSV]);
-                ++vrel;
-            }
-            const uint64_t olimit = obase + static_cast<uint64_t>(i) * OSZ;
-            while (orel < ow && os.A0 + static_cast<uint64_t>(orel + 1) * SC_OCHUNK <= olimit) {
-                mbar_arrive(&empty_o[orel % SC_NSO]);
-                ++orel;
-            }
-        }
-        // rb: the 16-byte-aligned row at or just before j; thread t owns rows
-        // [rb + t * SC_KR, rb + (t + 1) * SC_KR).
-        const int64_t rb = j - static_cast<int64_t>(((vbase >> 2) + static_cast<uint64_t>(j)) & 3);
-        const int nE = static_cast<int>(i_end - i);
-
-        // ---- pass 1: mark segment starts (and j) ------------------------------
-        for (int q = tid; q <= nE; q += SC_NT) {
-            const int64_t b = off_r(i + q);
-            if (b >= j && b < j_end) keep[b - rb] = 0u;
-        }
-        if (tid == 0 && j < j_end) keep[j - rb] = 0u;
-        named_bar_sync<SC_NT>();
-
-        // ---- pass 2: segmented scan of my rows --------------------------------
-        const int64_t blk = rb + static_cast<int64_t>(tid) * SC_KR;
-        const int32_t row0 = static_cast<int32_t>(blk - Rlo);    // CTA-relative row of my first row
-        uint32_t xb[SC_KR];
-        uint32_t kp[SC_KR];
-        {
-            const uint32_t at0 = ring_at(blk);
+            // write the running values back over rows < tr1 (later rows are the
+            // next tile's input; earlier rows are finished)
+            const int32_t hi = tr - lrow0;
+            if (hi >= SW_KR) {
 #pragma unroll
-            for (int q = 0; q < SC_KR / 4; ++q) {
-                const uint4 u = *reinterpret_cast<const uint4*>(vring + ((at0 + 16u * q) & (SC_VRING - 1)));
-                xb[4 * q + 0] = u.x;
-                xb[4 * q + 1] = u.y;
-                xb[4 * q + 2] = u.z;
-                xb[4 * q + 3] = u.w;
-                const uint4 k4 = *reinterpret_cast<const uint4*>(&keep[tid * SC_KR + 4 * q]);
-                kp[4 * q + 0] = k4.x;
-                kp[4 * q + 1] = k4.y;
-                kp[4 * q + 2] = k4.z;
-                kp[4 * q + 3] = k4.w;
-            }
-        }
-        Acc<T> acc = RD::ident();
-        bool fl = false;
-        int32_t rr[OP == OP_SUM ? 1 : SC_KR];
-#pragma unroll
-        for (int k = 0; k < SC_KR; ++k) {
-            const T x = from_bits<T>(xb[k]);
-            if constexpr (OP == OP_SUM) {
-                acc.v = add_wrap(from_bits<T>(bits_of(acc.v) & kp[k]), x);
-            } else {
-                const bool better = (OP == OP_MIN) ? (x < acc.v) : (x > acc.v);
-                if (kp[k] == 0u || acc.row < 0 || better) {
-                    acc.v = x;
-                    acc.row = row0 + k;
-                }
-                rr[k] = acc.row;
-            }
-            xb[k] = bits_of(acc.v);
-            fl = fl || (kp[k] == 0u);
-        }
-        {
-            // Write running values back over rows < j_end (rows >= j_end belong
-            // to the next tile; rows < j were finished by the previous tile).
-            const int64_t hi = j_end - blk;
-            const uint32_t at0 = ring_at(blk);
-            if (hi >= SC_KR) {
-#pragma unroll
-                for (int q = 0; q < SC_KR / 4; ++q) {
-                    *reinterpret_cast<uint4*>(vring + ((at0 + 16u * q) & (SC_VRING - 1))) =
+                for (int q = 0; q < SW_KR / 4; ++q)
+                    *reinterpret_cast<uint4*>(stage + lane * (SW_KR * 4) + 16 * q) =
                         make_uint4(xb[4 * q], xb[4 * q + 1], xb[4 * q + 2], xb[4 * q + 3]);
-                    if constexpr (OP != OP_SUM)
-                        *reinterpret_cast<int4*>(&argr[tid * SC_KR + 4 * q]) =
-                            make_int4(rr[4 * q], rr[4 * q + 1], rr[4 * q + 2], rr[4 * q + 3]);
+                if constexpr (OP != OP_SUM) {
+#pragma unroll
+                    for (int q = 0; q < SW_KR / 2; ++q)
+                        *reinterpret_cast<uint32_t*>(&argr[lrow0 + 2 * q]) =
+                            (static_cast<uint32_t>(static_cast<uint16_t>(rr[2 * q + 1])) << 16) |
+                            static_cast<uint16_t>(rr[2 * q]);
                 }
             } else if (hi > 0) {
 #pragma unroll
-                for (int k = 0; k < SC_KR; ++k) {
+                for (int k = 0; k < SW_KR; ++k) {
                     if (k < hi) {
-                        *reinterpret_cast<uint32_t*>(vring + ((at0 + 4u * k) & (SC_VRING - 1))) = xb[k];
-                        if constexpr (OP != OP_SUM) argr[tid * SC_KR + k] = rr[k];
+                        *reinterpret_cast<uint32_t*>(stage + (lrow0 + k) * 4) = xb[k];
+                        if constexpr (OP != OP_SUM) argr[lrow0 + k] = rr[k];
                     }
                 }
             }
-        }
-        // segmented scan of the thread totals across the warp
-        Acc<T> inc = acc;
-        bool fi = fl;
+            // segmented scan of the lane totals; X = exclusive prefix
+            Acc<T> inc = acc;
+            bool fi = w != 0u;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            Acc<T> pv;
-            pv.v = from_bits<T>(__shfl_up_sync(0xffffffffu, bits_of(inc.v), o));
-            pv.row = __shfl_up_sync(0xffffffffu, inc.row, o);
-            const bool pf = __shfl_up_sync(0xffffffffu, fi, o);
-            if (lane >= o) {
-                if (!fi) inc = RD::comb(pv, inc);
-                fi = fi || pf;
+            for (int o = 1; o < 32; o <<= 1) {
+                Acc<T> pv;
+                pv.v = from_bits<T>(__shfl_up_sync(0xffffffffu, bits_of(inc.v), o));
+                if constexpr (OP != OP_SUM) pv.row = __shfl_up_sync(0xffffffffu, inc.row, o);
+                else pv.row = -1;
+                const bool pf = __shfl_up_sync(0xffffffffu, fi, o);
+                if (lane >= o) {
+                    if (!fi) inc = RD::comb(pv, inc);
+                    fi = fi || pf;
+                }
             }
+            X.v = from_bits<T>(__shfl_up_sync(0xffffffffu, bits_of(inc.v), 1));
+            if constexpr (OP != OP_SUM) X.row = __shfl_up_sync(0xffffffffu, inc.row, 1);
+            if (lane == 0) X = RD::ident();
+            __syncwarp();
         }
-        Acc<T> ex;
-        ex.v = from_bits<T>(__shfl_up_sync(0xffffffffu, bits_of(inc.v), 1));
-        ex.row = __shfl_up_sync(0xffffffffu, inc.row, 1);
-        bool exf = __shfl_up_sync(0xffffffffu, fi, 1);
-        if (lane == 0) {
-            ex = RD::ident();
-            exf = false;
-        }
-        if (lane == 31) {
-            wv[warp] = inc.v;
-            wr[warp] = inc.row;
-            wf[warp] = fi ? 1 : 0;
-        }
-        named_bar_sync<SC_NT>();
-        {
-            Acc<T> pre = RD::ident();
-            for (int w2 = 0; w2 < warp; ++w2) {
-                Acc<T> a;
-                a.v = wv[w2];
-                a.row = wr[w2];
-                pre = wf[w2] ? a : RD::comb(pre, a);
-            }
-            const Acc<T> X = exf ? ex : RD::comb(pre, ex);
-            xv[tid] = X.v;
-            xr[tid] = X.row;
-        }
-        named_bar_sync<SC_NT>();
-
-        // ---- pass 3: one result per segment end; clear the marks --------------
-        const C carry_in = carry_buf[par];
-        auto running_at = [&](int64_t row, int64_t start) -> Acc<T> {
-            // running value at `row` of the run that starts at `start` (>= j);
-            // valid offsets give j <= row < j_end, the clamp only guards
-            // shared-memory indexing against malformed offsets
-            row = row < j ? j : (row >= j_end ? j_end - 1 : row);
-            const int64_t k = row - rb;
+        // running value at chunk row `k` (jr <= k < tr) of the run starting at
+        // chunk row `st`: the lane's running value there, joined with the owning
+        // lane's prefix when the run began in an earlier lane (every lane calls
+        // this together: it shuffles)
+        auto running_at = [&](int32_t k, int32_t st) -> Acc<T> {
+            if (!has_rows) return RD::ident();   // uniform across the warp
+            k = k < jr ? jr : (k >= tr ? tr - 1 : k);
+            const int o = k / SW_KR;
+            Acc<T> Xo;
+            Xo.v = from_bits<T>(__shfl_sync(0xffffffffu, bits_of(X.v), o));
+            if constexpr (OP != OP_SUM) Xo.row = __shfl_sync(0xffffffffu, X.row, o);
+            else Xo.row = -1;
             Acc<T> P;
-            P.v = *reinterpret_cast<const T*>(vring + ring_at(row));
+            P.v = *reinterpret_cast<const T*>(stage + k * 4);
             if constexpr (OP == OP_SUM) {
                 P.row = -1;
             } else {
-                P.row = argr[k];
+                P.row = static_cast<int32_t>(argr[k]) + crow_u;
             }
-            const int t2 = static_cast<int>(k / SC_KR);
-            if (start < rb + static_cast<int64_t>(t2) * SC_KR) {
-                Acc<T> X;
-                X.v = xv[t2];
-                X.row = xr[t2];
-                P = RD::comb(X, P);
-            }
-            return P;
+            return st < o * SW_KR ? RD::comb(Xo, P) : P;
         };
-        for (int q = tid; q <= nE; q += SC_NT) {
-            const int64_t s = i + q;
-            const int64_t b = off_r(s);
-            if (b >= j && b < j_end) keep[b - rb] = ~0u;
-            if (q == 0 && j < j_end) keep[j - rb] = ~0u;
-            if (q < nE) {
-                const int64_t e = off_r(s + 1);
-                C R = CO::ident();
-                if (e > b) {
-                    if (e - 1 < j) {
-                        R = carry_in;    // ended exactly at the tile start
-                    } else {
-                        const Acc<T> P = running_at(e - 1, b > j ? b : j);
-                        R = b < j ? CO::then(carry_in, P) : CO::from(P);
-                    }
-                }
-                const int64_t len = e > b ? e - b : 0;
-                if (head_pending && s == Ilo) {
-                    // began in an earlier CTA: leave the head partial, join the ticket
-                    if constexpr (OP == OP_SUM && kIsFloat<T>) heads[cta] = to_part(R);
-                    else heads[cta] = to_part<T, OP>(R, Rlo);
+        // 3. ends
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            if (k == 1 && n_e <= 32) break;
+            const int idx = 32 * k + lane;
+            const bool valid = idx < n_e;
+            const int64_t s = es + idx;
+            const int64_t ob = valid ? B[k] : j;
+            const int64_t oe = valid ? E[k] : j;
+            const bool rows_here = valid && has_rows && oe > ob && oe - 1 >= j;
+            const int32_t kl = rows_here ? static_cast<int32_t>(oe - 1 - crow0) : jr;
+            const int32_t st = static_cast<int32_t>((ob > j ? ob : j) - crow0);
+            const Acc<T> P = running_at(kl, st);
+            const int64_t len = oe > ob ? oe - ob : 0;
+            bool last = false;
+            int pc = 0;
+            if (valid) {
+                if (head_pending && s == Iu) {
+                    // began in an earlier unit: leave the head partial, join the ticket
+                    const C R = rows_here ? CO::then(carry, P) : carry;
+                    if constexpr (OP == OP_SUM && kIsFloat<T>) heads[u_me] = to_part(R);
+                    else heads[u_me] = to_part<T, OP>(R, Ru);
                     __threadfence();
-                    const int64_t f = b - o0 + Ilo;
-                    int pc = static_cast<int>(f / W);
-                    pc = pc < 0 ? 0 : (pc > cta ? cta : pc);
-                    if (ticket_arrive(p.ws_tickets, cta, cta - pc + 1, p.gen)) {
-                        __threadfence();
-                        combine_store<T, OP>(p, tails, heads, pc, cta, s, len, 0, 1);
-                    }
+                    const int64_t f = ob - o0 + Iu;
+                    pc = static_cast<int>(f / Wu);
+                    pc = pc < 0 ? 0 : (pc > u_me ? static_cast<int>(u_me) : pc);
+                    last = ticket_arrive(p.ws_tickets, static_cast<int>(u_me),
+                                         static_cast<int>(u_me) - pc + 1, p.gen);
+                    if (last) __threadfence();
                 } else {
                     T v;
                     int64_t a;
-                    if constexpr (OP == OP_SUM && kIsFloat<T>) {
-                        finish_carry(R, len, mean, v);
+                    if (len == 0) {
+                        v = T(0);
                         a = -1;
+                    } else if (ob >= j) {
+                        finish_acc<T, OP>(P, len, mean, Ru, v, a);   // began in this tile
                     } else {
-                        finish_acc<T, OP>(R, len, mean, Rlo, v, a);
+                        const C R = rows_here ? CO::then(carry, P) : carry;
+                        if constexpr (OP == OP_SUM && kIsFloat<T>) {
+                            finish_carry(R, len, mean, v);
+                            a = -1;
+                        } else {
+                            finish_acc<T, OP>(R, len, mean, Ru, v, a);
+                        }
                     }
                     out[s] = v;
                     if (want_arg) p.out_arg[s] = a;
                 }
-            } else {
-                // the segment left open (i_end): its running value into the carry
-                C nc = CO::ident();
-                if (i_end < S) {
-                    const int64_t st = b > j ? b : j;
-                    if (st < j_end) {
-                        const Acc<T> P = running_at(j_end - 1, st);
-                        nc = b < j ? CO::then(carry_in, P) : CO::from(P);
-                    } else {
-                        nc = b < j ? carry_in : CO::ident();
-                    }
+            }
+            if (head_pending && k == 0) {
+                // the unit's first end sat on lane 0
+                last = __shfl_sync(0xffffffffu, last, 0);
+                pc = __shfl_sync(0xffffffffu, pc, 0);
+                const int64_t hl = __shfl_sync(0xffffffffu, len, 0);
+                if (last)
+                    warp_combine_store<T, OP>(p, tails, heads, pc, static_cast<int>(u_me), Iu, hl, lane);
+            }
+        }
+        if (n_e > 0) head_pending = false;
+        // the segment left open, es + n_e, starts at offsets[es + n_e]
+        {
+            const int l = (n_e - 1) & 31;
+            const int64_t e0 = __shfl_sync(0xffffffffu, E[0], l);
+            const int64_t e1 = __shfl_sync(0xffffffffu, E[1], l);
+            const int64_t bo = n_e == 0 ? b_es : (n_e <= 32 ? e0 : e1);
+            const int64_t sto = bo > j ? bo : j;
+            const bool rows_open = has_rows && sto < tr1;
+            const Acc<T> P = running_at(tr - 1, static_cast<int32_t>(sto - crow0));
+            if (rows_open)
+                carry = bo < j ? CO::then(carry, P) : CO::from(P);
+            else if (!(bo < j))
+                carry = CO::ident();
+            b_es = bo;
+        }
+        j = tr1;
+        es += n_e;
+        __syncwarp();
+        // hand back offsets chunks that hold only entries before es
+        if (lane == 0) {
+            while (odone < ow && os.A0 + static_cast<uint64_t>(odone + 1) * SW_OCHUNK <=
+                                     obase + static_cast<uint64_t>(es) * OSZ) {
+                if (o_issued < os.nch) {
+                    issue_chunk(os, o_issued, oring, SW_ORING, SW_OCHUNK, &fo[o_issued % SW_NSO], policy);
+                    ++o_issued;
                 }
-                carry_buf[par ^ 1] = nc;
+                ++odone;
             }
         }
-        if (i_end > i) head_pending = false;
-        par ^= 1;
-        d = d_end;
-        i = i_end;
-        j = j_end;
+        odone = __shfl_sync(0xffffffffu, odone, 0);
+        o_issued = __shfl_sync(0xffffffffu, o_issued, 0);
     }
+    v_issued = __shfl_sync(0xffffffffu, v_issued, 0);
 
-    // ---- a6: the segment still open at the end of the range ------------------
-    named_bar_sync<SC_NT>();
-    if (tid == 0 && Ihi < S) {
-        const int64_t ob = clamp_off(__ldg(&offs[Ihi]), N);
-        if (ob < Rhi) {
-            const C cf = carry_buf[par];
-            if constexpr (OP == OP_SUM && kIsFloat<T>) tails[cta] = to_part(cf);
-            else tails[cta] = to_part<T, OP>(cf, Rlo);
-            __threadfence();
-            const int64_t oe = clamp_off(__ldg(&offs[Ihi + 1]), N);
-            const int64_t f = ob - o0 + Ihi;
-            const int64_t e = (oe > ob ? oe : ob) - o0 + Ihi;
-            int pc = static_cast<int>(f / W);
-            int qc = static_cast<int>(e / W);
-            pc = pc < 0 ? 0 : (pc > cta ? cta : pc);
-            qc = qc <= cta ? cta + 1 : qc;
-            if (qc < p.P && ticket_arrive(p.ws_tickets, qc, qc - pc + 1, p.gen)) {
+    // ---- a6: the segment still open at the end of the unit -------------------------
+    if (ok && Iu2 < S) {
+        const int64_t ob = clamp_off(__ldg(&offs[Iu2]), N);
+        if (ob < Ru2) {
+            bool last = false;
+            int pc = 0, qc = 0;
+            if (lane == 0) {
+                if constexpr (OP == OP_SUM && kIsFloat<T>) tails[u_me] = to_part(carry);
+                else tails[u_me] = to_part<T, OP>(carry, Ru);
                 __threadfence();
-                combine_store<T, OP>(p, tails, heads, pc, qc, Ihi, oe > ob ? oe - ob : 0, 0, 1);
+                const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
+                const int64_t f = ob - o0 + Iu2;
+                const int64_t e = (oe > ob ? oe : ob) - o0 + Iu2;
+                pc = static_cast<int>(f / Wu);
+                qc = static_cast<int>(e / Wu);
+                pc = pc < 0 ? 0 : (pc > u_me ? static_cast<int>(u_me) : pc);
+                qc = qc <= u_me ? static_cast<int>(u_me) + 1 : qc;
+                last = qc < U && ticket_arrive(p.ws_tickets, qc, qc - pc + 1, p.gen);
+                if (last) __threadfence();
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            pc = __shfl_sync(0xffffffffu, pc, 0);
+            qc = __shfl_sync(0xffffffffu, qc, 0);
+            if (last) {
+                const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
+                warp_combine_store<T, OP>(p, tails, heads, pc, qc, Iu2, oe > ob ? oe - ob : 0, lane);
             }
         }
+    }
+    // every copy this warp started must land before it exits
+    if (lane == 0) {
+        for (int64_t k = m + (m_ready ? 1 : 0); k < v_issued; ++k)
+            wait_bounded(&fv[k % SW_NSV], static_cast<uint32_t>((k / SW_NSV) & 1), p.status,
+                         STATUS_DRAIN_TIMEOUT);
+        for (int64_t k = ow; k < o_issued; ++k)
+            wait_bounded(&fo[k % SW_NSO], static_cast<uint32_t>((k / SW_NSO) & 1), p.status,
+                         STATUS_DRAIN_TIMEOUT);
     }
 }
 
