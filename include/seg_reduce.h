@@ -59,7 +59,8 @@ typedef enum {
     SEG_ERR_UNSUPPORTED = 2,      /* mean on integer values, F above SEG_MAX_FEATURES */
     SEG_ERR_OUT_OF_MEMORY = 3,    /* the scratch buffer could not be allocated */
     SEG_ERR_CUDA = 4,             /* a CUDA runtime call or a launch failed */
-    SEG_ERR_DEVICE_TIMEOUT = 5    /* a device-side bounded wait ran out (see seg_reduce_device_status) */
+    SEG_ERR_DEVICE_TIMEOUT = 5,   /* a device-side bounded wait ran out (see seg_reduce_device_status) */
+    SEG_ERR_SCRATCH_LIMIT = 6     /* seg_reduce_noalloc: the call needs more than SEG_NOALLOC_SCRATCH_BYTES */
 } seg_status_t;
 
 /* Largest F (columns per row) that seg_reduce accepts. */
@@ -136,6 +137,65 @@ seg_status_t seg_reduce_plan(seg_dtype_t dtype, int64_t F, int64_t num_values,
                              int64_t num_segments, seg_op_t op,
                              uint64_t values_addr, int32_t sm_count,
                              seg_plan_t *plan);
+
+/*
+ * seg_reduce_noalloc -- seg_reduce without any allocation.
+ *
+ * The reduction pages have no counterpart of this call: it exists for
+ * callers that may not allocate device memory at the moment they reduce,
+ * for example a runtime whose device memory is all reserved ahead of time by
+ * its own arena, or a latency-critical loop that must not touch the
+ * stream-ordered allocator pool (growing or trimming that pool can add
+ * synchronisation and jitter).  It computes exactly what seg_reduce computes
+ * for the same arguments (same kernels, same launch shape, same summation
+ * order, so results are bitwise equal to seg_reduce's), but the scratch it
+ * needs (ticket words and cross-unit partials) lives in a fixed array of
+ * SEG_NOALLOC_SCRATCH_BYTES bytes of static device memory inside the library,
+ * one per device, and no call to cudaMalloc, cudaMallocAsync, cudaFree or any
+ * other allocating routine is made.
+ *
+ * Arguments are those of seg_reduce plus:
+ *   status_word   device, caller-owned, 4-byte aligned, or NULL.  A kernel
+ *                 whose bounded wait runs out ORs a nonzero code into it
+ *                 (the call's outputs are then incomplete); the library never
+ *                 clears it.  NULL sends such codes to a word inside the
+ *                 library that nothing reads.  seg_reduce_device_status does
+ *                 not see errors of this call.
+ *
+ * Limit.  The scratch a launch needs grows with the grid and, for row
+ * tensors, with F: (ticket words: SM count * 128 bytes rounded up to 256) +
+ * (partials: 2 * grid * 16 * 16 bytes for F == 1, 2 * grid * F * 16 bytes
+ * for F > 1).  On a 152-SM GPU every F == 1 call fits, and F > 1 fits up to
+ * F = 858 at a full grid (seg_reduce_plan reports workspace_bytes).  A call
+ * that would need more returns SEG_ERR_SCRATCH_LIMIT before launching
+ * anything; use seg_reduce for it.
+ *
+ * Set-up.  The first call on each device looks up the array's address
+ * (cudaGetSymbolAddress, with that device current), clears its ticket words
+ * (a stream-ordered memset on `stream`) and waits for `stream` to finish
+ * that; the first call of each kernel shape on a device also sets the
+ * kernel's shared-memory attribute.  Make one call of each shape you will
+ * use before any stream capture.  After that a call only enqueues one
+ * memset every 2^32 - 1 calls (when the generation tag of the ticket words
+ * wraps) plus the kernel launch.
+ *
+ * What must start at zero: only the ticket words (the first
+ * SM count * 128 bytes of the array); the library zeroes them itself as
+ * described above.  Partials are always written before they are read.
+ *
+ * Concurrency.  All calls on one device share the one array.  Two calls
+ * whose kernels can overlap in time (different streams without an ordering
+ * between them, or different host threads) race on it and give wrong
+ * results; order them on one stream, or synchronise between them.
+ */
+#define SEG_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+seg_status_t seg_reduce_noalloc(const void *values, seg_dtype_t dtype, int64_t F,
+                                int64_t num_values, const void *offsets,
+                                seg_offset_dtype_t offsets_dtype,
+                                int64_t num_segments, seg_op_t op, void *out,
+                                int64_t *out_arg, unsigned int *status_word,
+                                seg_stream_t stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t seg_reduce_version(void);

@@ -23,7 +23,7 @@ import threading
 __all__ = [
     "seg_reduce", "segment_sum_csr", "segment_mean_csr", "segment_min_csr",
     "segment_max_csr", "plan", "device_status", "library_path", "load_library",
-    "SegReduceError",
+    "SegReduceError", "seg_reduce_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,9 +34,11 @@ SEG_U32, SEG_S32, SEG_F32 = 0, 1, 2
 SEG_OFF_U32, SEG_OFF_I64 = 0, 1
 OPS = {"sum": 0, "min": 1, "max": 2, "mean": 3}
 STATUS = {0: "SEG_OK", 1: "SEG_ERR_INVALID_ARGUMENT", 2: "SEG_ERR_UNSUPPORTED",
-          3: "SEG_ERR_OUT_OF_MEMORY", 4: "SEG_ERR_CUDA", 5: "SEG_ERR_DEVICE_TIMEOUT"}
+          3: "SEG_ERR_OUT_OF_MEMORY", 4: "SEG_ERR_CUDA", 5: "SEG_ERR_DEVICE_TIMEOUT",
+          6: "SEG_ERR_SCRATCH_LIMIT"}
 EXPORTED = ("seg_reduce", "seg_reduce_strerror", "seg_reduce_device_status",
-            "seg_reduce_plan", "seg_reduce_version")
+            "seg_reduce_plan", "seg_reduce_version", "seg_reduce_noalloc")
+NOALLOC_SCRATCH_BYTES = 4 << 20   # SEG_NOALLOC_SCRATCH_BYTES
 
 
 class SegReduceError(RuntimeError):
@@ -85,6 +87,9 @@ def load_library(path: str | None = None):
                                         ctypes.c_uint64, i32, ctypes.POINTER(_Plan)]
         lib.seg_reduce_version.restype = i32
         lib.seg_reduce_version.argtypes = []
+        lib.seg_reduce_noalloc.restype = ctypes.c_int
+        lib.seg_reduce_noalloc.argtypes = [vp, ctypes.c_int, i64, i64, vp, ctypes.c_int, i64,
+                                           ctypes.c_int, vp, vp, vp, vp]
         if path is None:
             _lib = lib
         return lib
@@ -182,6 +187,64 @@ def seg_reduce(values, offsets, op: str = "sum", out=None, out_arg=None, with_ar
     if rc != 0:
         raise SegReduceError(rc, "seg_reduce")
     return (out, out_arg) if want_arg else out
+
+
+def seg_reduce_noalloc(values, offsets, op: str, out, out_arg=None, status_word=None,
+                       stream=None):
+    """``seg_reduce`` through the library's allocation-free entry point.
+
+    For callers that may not allocate device memory when they reduce: neither
+    the library (its scratch is a fixed static device array of
+    ``NOALLOC_SCRATCH_BYTES``) nor this wrapper allocates anything, so ``out``
+    (and ``out_arg`` to receive min / max rows) must be passed preallocated.
+    ``status_word`` is an optional caller-owned int32 / uint32 CUDA tensor of
+    one element that a timed-out device wait ORs a code into.  Calls whose
+    kernels could overlap in time (other streams, other threads) race on the
+    one array per device.  Raises ``SegReduceError`` with
+    ``SEG_ERR_SCRATCH_LIMIT`` when the call needs more scratch than the array
+    holds (large grids with wide rows).  Returns what ``seg_reduce`` returns.
+    """
+    torch = _torch()
+    if op not in OPS:
+        raise ValueError(f"op must be one of {sorted(OPS)}")
+    if not values.is_cuda or not offsets.is_cuda:
+        raise ValueError("values and offsets must be CUDA tensors (there is no CPU path)")
+    if values.device != offsets.device:
+        raise ValueError("values and offsets must be on the same device")
+    if values.dim() not in (1, 2) or offsets.dim() != 1 or offsets.numel() < 1:
+        raise ValueError("values must be [N] or [N, F] and offsets [S+1]")
+    if not values.is_contiguous() or not offsets.is_contiguous():
+        raise ValueError("values and offsets must be contiguous")
+    n = values.shape[0]
+    feat = 1 if values.dim() == 1 else values.shape[1]
+    s = offsets.numel() - 1
+    oshape = (s,) if values.dim() == 1 else (s, feat)
+    if (out is None or tuple(out.shape) != oshape or out.dtype != values.dtype
+            or not out.is_contiguous() or out.device != values.device):
+        raise ValueError(f"out must be a preallocated contiguous {values.dtype} CUDA tensor "
+                         f"of shape {oshape}")
+    if out_arg is not None and (op not in ("min", "max") or tuple(out_arg.shape) != oshape
+                                or out_arg.dtype != torch.int64 or not out_arg.is_contiguous()
+                                or out_arg.device != values.device):
+        raise ValueError(f"out_arg must be a contiguous int64 CUDA tensor of shape {oshape}, "
+                         "for min / max only")
+    if status_word is not None and (status_word.numel() != 1 or status_word.element_size() != 4
+                                    or status_word.device != values.device):
+        raise ValueError("status_word must be a one-element 32-bit CUDA tensor")
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream(values.device)
+    with torch.cuda.device(values.device):
+        rc = lib.seg_reduce_noalloc(
+            values.data_ptr() if n else None, _value_code(values), feat, n,
+            offsets.data_ptr(), _offset_code(offsets), s, OPS[op],
+            out.data_ptr() if s else None,
+            out_arg.data_ptr() if (out_arg is not None and s) else None,
+            status_word.data_ptr() if status_word is not None else None,
+            ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SegReduceError(rc, "seg_reduce_noalloc")
+    return (out, out_arg) if out_arg is not None else out
 
 
 def segment_sum_csr(src, indptr):

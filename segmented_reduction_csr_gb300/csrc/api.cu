@@ -170,6 +170,63 @@ seg_status_t scratch_for(int dev, cudaStream_t stream, size_t bytes, Scratch** o
     return SEG_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Fixed scratch for seg_reduce_noalloc: static device memory, one array per
+// device (a __device__ variable exists once in every context), so that call
+// never allocates.  Its ticket words must read zero before the first launch;
+// set-up clears them once per device.
+
+static __device__ __align__(256) unsigned char g_fixed_scratch[SEG_NOALLOC_SCRATCH_BYTES];
+static __device__ unsigned int g_fixed_status;   // device errors when the caller passes no word
+
+constexpr int kMaxKernels = 128;   // compiled kernels: 3 dtypes x 3 ops x 2 offset types x 5 shapes
+
+struct FixedState {
+    bool init = false;
+    int sm_count = 0;
+    unsigned char* scratch = nullptr;
+    unsigned int* status = nullptr;
+    uint32_t gen = 0;
+    const void* configured[kMaxKernels] = {};
+    int n_configured = 0;
+};
+
+std::mutex g_fixed_mu;
+FixedState g_fixed[kMaxDevices];
+
+// First call on a device: SM count, the arrays' addresses, zeroed ticket
+// words (waited for, so that every later launch on any stream sees zeros).
+seg_status_t fixed_state(int dev, cudaStream_t stream, FixedState** out) {
+    if (dev < 0 || dev >= kMaxDevices) return SEG_ERR_CUDA;
+    FixedState& fs = g_fixed[dev];
+    if (!fs.init) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SEG_ERR_CUDA;
+        void* scratch = nullptr;
+        void* status = nullptr;
+        if (cudaGetSymbolAddress(&scratch, g_fixed_scratch) != cudaSuccess ||
+            cudaGetSymbolAddress(&status, g_fixed_status) != cudaSuccess) {
+            cudaGetLastError();
+            return SEG_ERR_CUDA;
+        }
+        const int64_t tickets = ticket_region_bytes(sms);
+        if (tickets > int64_t(SEG_NOALLOC_SCRATCH_BYTES)) return SEG_ERR_SCRATCH_LIMIT;
+        if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(tickets), stream) != cudaSuccess ||
+            cudaMemsetAsync(status, 0, sizeof(unsigned int), stream) != cudaSuccess ||
+            cudaStreamSynchronize(stream) != cudaSuccess) {
+            cudaGetLastError();
+            return SEG_ERR_CUDA;
+        }
+        fs.sm_count = sms;
+        fs.scratch = static_cast<unsigned char*>(scratch);
+        fs.status = static_cast<unsigned int*>(status);
+        fs.init = true;
+    }
+    *out = &fs;
+    return SEG_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -272,6 +329,7 @@ const char* seg_reduce_strerror(seg_status_t status) {
         case SEG_ERR_OUT_OF_MEMORY: return "out of device memory for scratch";
         case SEG_ERR_CUDA: return "CUDA runtime error";
         case SEG_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
+        case SEG_ERR_SCRATCH_LIMIT: return "the call needs more scratch than the fixed no-allocation array holds";
         default: return "unknown status";
     }
 }
@@ -293,6 +351,100 @@ seg_status_t seg_reduce_device_status(seg_stream_t stream_) {
     if (cudaMemcpy(&h, word, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SEG_ERR_CUDA;
     if (h != 0 && cudaMemset(word, 0, sizeof(h)) != cudaSuccess) return SEG_ERR_CUDA;
     return h ? SEG_ERR_DEVICE_TIMEOUT : SEG_OK;
+}
+
+seg_status_t seg_reduce_noalloc(const void* values, seg_dtype_t dtype, int64_t F,
+                                int64_t num_values, const void* offsets,
+                                seg_offset_dtype_t offsets_dtype, int64_t num_segments, seg_op_t op,
+                                void* out, int64_t* out_arg, unsigned int* status_word,
+                                seg_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const int64_t S = num_segments;
+    // The same host-visible checks as seg_reduce; nothing is launched when one fails.
+    if (dtype != SEG_U32 && dtype != SEG_S32 && dtype != SEG_F32) return SEG_ERR_INVALID_ARGUMENT;
+    if (offsets_dtype != SEG_OFF_U32 && offsets_dtype != SEG_OFF_I64) return SEG_ERR_INVALID_ARGUMENT;
+    if (op != SEG_SUM && op != SEG_MIN && op != SEG_MAX && op != SEG_MEAN) return SEG_ERR_INVALID_ARGUMENT;
+    if (F < 1 || num_values < 0 || S < 0) return SEG_ERR_INVALID_ARGUMENT;
+    if (op == SEG_MEAN && dtype != SEG_F32) return SEG_ERR_UNSUPPORTED;
+    if (F > SEG_MAX_FEATURES) return SEG_ERR_UNSUPPORTED;
+    if ((op == SEG_SUM || op == SEG_MEAN) && out_arg != nullptr) return SEG_ERR_INVALID_ARGUMENT;
+    if (S == 0) return SEG_OK;
+    if (!offsets || !out || (num_values > 0 && !values)) return SEG_ERR_INVALID_ARGUMENT;
+    const size_t osz = offsets_dtype == SEG_OFF_U32 ? 4 : 8;
+    if (reinterpret_cast<uintptr_t>(values) % 4 || reinterpret_cast<uintptr_t>(out) % 4 ||
+        reinterpret_cast<uintptr_t>(offsets) % osz || reinterpret_cast<uintptr_t>(out_arg) % 8 ||
+        reinterpret_cast<uintptr_t>(status_word) % 4)
+        return SEG_ERR_INVALID_ARGUMENT;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SEG_ERR_CUDA;
+
+    std::lock_guard<std::mutex> lock(g_fixed_mu);
+    FixedState* fs = nullptr;
+    seg_status_t st = fixed_state(dev, stream, &fs);
+    if (st != SEG_OK) return st;
+
+    seg_plan_t pl;
+    st = plan_launch(dtype, F, num_values, offsets_dtype, S, op,
+                     reinterpret_cast<uint64_t>(values), fs->sm_count, &pl);
+    if (st != SEG_OK) return st;
+    if (pl.workspace_bytes > int64_t(SEG_NOALLOC_SCRATCH_BYTES)) return SEG_ERR_SCRATCH_LIMIT;
+
+    const int kop = op == SEG_MIN ? OP_MIN : (op == SEG_MAX ? OP_MAX : OP_SUM);
+    const int i64 = offsets_dtype == SEG_OFF_I64 ? 1 : 0;
+    const void* fn = dtype == SEG_U32   ? pick_kernel_u32(kop, i64, pl.kernel_variant)
+                     : dtype == SEG_S32 ? pick_kernel_s32(kop, i64, pl.kernel_variant)
+                                        : pick_kernel_f32(kop, i64, pl.kernel_variant);
+    if (!fn) return SEG_ERR_UNSUPPORTED;
+    bool configured = false;
+    for (int k = 0; k < fs->n_configured; ++k) configured = configured || fs->configured[k] == fn;
+    if (!configured) {
+        if (fs->n_configured >= kMaxKernels) return SEG_ERR_UNSUPPORTED;
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(pl.smem_bytes)) != cudaSuccess) {
+            cudaGetLastError();
+            return SEG_ERR_CUDA;
+        }
+        fs->configured[fs->n_configured++] = fn;
+    }
+    // A new generation tag per call retires the previous call's ticket
+    // counts; when the tag would wrap, the ticket words are cleared instead.
+    if (fs->gen == UINT32_MAX) {
+        if (cudaMemsetAsync(fs->scratch, 0, static_cast<size_t>(ticket_region_bytes(fs->sm_count)),
+                            stream) != cudaSuccess) {
+            cudaGetLastError();
+            return SEG_ERR_CUDA;
+        }
+        fs->gen = 0;
+    }
+    fs->gen += 1;
+
+    Params prm;
+    prm.values = values;
+    prm.offsets = offsets;
+    prm.out = out;
+    prm.out_arg = (op == SEG_MIN || op == SEG_MAX) ? out_arg : nullptr;
+    prm.N = num_values;
+    prm.S = S;
+    prm.F = static_cast<int32_t>(F);
+    prm.G = pl.slot_threads;
+    prm.K = pl.items_per_slot;
+    prm.max_ends = pl.max_ends;
+    prm.P = pl.grid;
+    prm.mean = op == SEG_MEAN ? 1 : 0;
+    prm.ws_tickets = reinterpret_cast<unsigned long long*>(fs->scratch);
+    prm.ws_parts = fs->scratch + ticket_region_bytes(fs->sm_count);
+    prm.status = status_word != nullptr ? status_word : fs->status;
+    prm.gen = fs->gen;
+
+    void* args[] = {&prm};
+    const cudaError_t e = cudaLaunchKernel(fn, dim3(pl.grid), dim3(pl.block), args,
+                                           static_cast<size_t>(pl.smem_bytes), stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SEG_ERR_CUDA;
+    }
+    return SEG_OK;
 }
 
 int32_t seg_reduce_version(void) { return kVersion; }
