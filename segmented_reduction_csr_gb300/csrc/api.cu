@@ -55,16 +55,20 @@ seg_status_t plan_launch(seg_dtype_t dtype, int64_t F, int64_t num_values,
     std::memset(pl, 0, sizeof(*pl));
     const int64_t items = num_values + S;
     if (F == 1) {
-        // the scalar kernel: SW_NW warp units per CTA, each at least two chunks of rows
+        // the scalar kernel: SW_NW warp units per CTA, each at least two chunks of
+        // rows; a segment end weighs SW_CW rows in the partition
+        const int64_t witems = num_values + int64_t(SW_CW) * S;
         const int64_t per_cta = int64_t(SW_NW) * SW_TROWS * 2;
-        const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(sm_count, ceil_div(items, per_cta)));
+        const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(sm_count, ceil_div(witems, per_cta)));
+        // a unit's rows are addressed with 32-bit offsets inside the unit
+        if (ceil_div(witems, grid * SW_NW) + 16 >= int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;
         pl->grid = static_cast<int32_t>(grid);
         pl->block = SW_NTHREADS;
         pl->slot_threads = 1;
         pl->items_per_slot = SW_KR;
         pl->vec = 1;
         pl->vecs_per_thread = 1;
-        pl->max_ends = SW_EMAX;
+        pl->max_ends = SW_EMAXT;
         pl->kernel_variant = SHAPE_SCALAR;
         pl->smem_bytes = SW_SMEM;
         pl->workspace_bytes = ticket_region_bytes(sm_count) + 2 * grid * SW_NW * int64_t(sizeof(PartElem));

@@ -1,32 +1,39 @@
 // seg_scalar.cuh -- the scalar kernel: F == 1 vectors of uint32, int32 or
 // float32 (GPUSegmentedReduction's "packed scalar values").
 //
-// Work split.  The merge path of rows and segment ends is cut into units of
-// equal length, one unit per warp (SW_NW warps per CTA, one CTA per SM).  A
-// CTA finds the SW_NW + 1 unit boundaries it needs with one cooperative
-// search; after that every warp runs on its own: no CTA barrier in the main
-// loop, so the latency of one warp's steps hides behind the others.
+// Work split.  Rows and segment ends form one merged sequence in which a row
+// weighs 1 and a segment end weighs SW_CW (an end costs about that many rows
+// of work: its offsets load, its lookup and its store).  The sequence is cut
+// into units of equal weight, one unit per warp (SW_NW warps per CTA, one CTA
+// per SM), so skewed length distributions balance.  A CTA finds the SW_NW + 1
+// unit boundaries it needs with one cooperative search; after that every warp
+// runs on its own: no CTA barrier in the main loop.
 //
 // Per warp.  Lane 0 streams the unit's rows (SW_VCHUNK-byte chunks, SW_NSV
-// stages) and offsets (a SW_NSO-stage ring) into the warp's shared memory
-// with 1-D bulk copies, refilling a stage as soon as the warp is done with it.
-// A tile is the rows of one chunk plus the segment ends that fall in them (at
-// most SW_EMAX ends; a chunk with more is split into several tiles):
+// stages, with the next chunks prefetched into L2 so that a refill finds them
+// there) and offsets (a SW_NSO-stage ring) into the warp's shared memory with
+// 1-D bulk copies, refilling a stage as soon as the warp is done with it.
+// A tile is the rows of one chunk plus the segment ends that fall in them (up
+// to SW_EMAXT ends; a chunk with more, which takes many empty segments, is
+// split into several tiles):
 //
-//  1. marks: every lane takes segment ends and sets the bit of the row where
-//     the next segment starts (a 20-bit word per lane), plus the tile's first row;
-//  2. rows: lane l owns rows [20 l, 20 l + 20) of the chunk, loads them with
-//     128-bit shared loads (the 80-byte lane stride makes them conflict free),
-//     runs an inclusive segmented scan in registers (sum: restart at a mark;
-//     min / max: strict compare, restart at a mark; rows arrive in order so
-//     ties keep the lower row) and writes the running values back;  a
-//     segmented shuffle scan over the lanes gives each lane the running value
-//     of the rows before it;
-//  3. ends: every lane takes a segment end; its result is the running value at
-//     the segment's last row, joined with the owning lane's prefix (a shuffle)
-//     when the segment started in an earlier lane, and with the warp's carry
-//     when it started in an earlier tile.  Consecutive lanes store consecutive
-//     segments.  The carry of the segment left open is taken the same way.
+//  * a chunk that no segment end touches is summed as a whole: every lane
+//    folds its rows, then a fixed butterfly over the lanes;
+//  * otherwise: start flags (a byte per row: the tile's first row and, for
+//    each segment end, the row where the next segment starts); an inclusive
+//    segmented scan of each lane's SW_KR rows, a quad at a time (128-bit
+//    shared loads; the 144-byte lane stride keeps them conflict free), with
+//    the running values written back over the rows; a segmented shuffle scan
+//    of the lane totals, whose exclusive prefixes go to shared memory.  Then
+//    lanes take 32 segment ends at a time: the running value at the segment's last row,
+//    joined with the owning lane's prefix when the segment started in an
+//    earlier lane, and with the warp's carry when it started in an earlier
+//    tile.  Consecutive lanes store consecutive segments.
+//
+// The carry of the segment left open at a tile's end is kept by every lane;
+// float sums carry a compensated pair (TwoSum), so long chains of tiles add
+// no float32 error.  Rows are int32 offsets from the unit's first row (the
+// planner keeps a unit below 2^31 rows).
 //
 // A segment that crosses units leaves per-unit partials in scratch; the last
 // unit to arrive (atomic ticket, no waiting) combines them in unit order with
@@ -38,37 +45,41 @@ namespace segred {
 
 constexpr int SW_NW = 16;                      // warps (units) per CTA
 constexpr int SW_NTHREADS = SW_NW * 32;
-constexpr int SW_KR = 20;                      // rows per lane per tile (SW_KR / 4 odd)
+constexpr int SW_CW = 4;                       // merge-path weight of a segment end, in rows
+constexpr int SW_KR = 36;                      // rows per lane per tile
+constexpr int SW_Q = SW_KR / 4;                // quads per lane
 constexpr int SW_TROWS = 32 * SW_KR;           // rows per value chunk
 constexpr uint32_t SW_VCHUNK = SW_TROWS * 4;   // bytes per value chunk
-constexpr int SW_NSV = 3;                      // value stages per warp
+constexpr int SW_NSV = 2;                      // value stages per warp
 constexpr uint32_t SW_OCHUNK = 512;            // bytes per offsets chunk
 constexpr int SW_NSO = 4;                      // offsets stages per warp
 constexpr uint32_t SW_ORING = SW_OCHUNK * SW_NSO;
-constexpr int SW_EMAX = 64;                    // segment ends per tile (two per lane)
+constexpr int SW_EMAXT = 160;                  // segment ends per tile
 constexpr int SW_NDIAG = SW_NW + 1;            // unit boundaries per CTA
 constexpr int SW_GRID = 1024;                  // first-round probes, shared by all CTAs
 constexpr int SW_PROBES = 60;                  // later-round probes per boundary
-static_assert((SW_KR / 4) % 2 == 1, "conflict-free 128-bit row loads need SW_KR / 4 odd");
+static_assert(SW_Q % 2 == 1, "conflict-free 128-bit row loads need SW_KR / 4 odd");
 static_assert(SW_NDIAG * SW_PROBES <= 2 * SW_NTHREADS, "two probes per thread per round");
-static_assert((SW_EMAX + 1) * 8 + SW_OCHUNK <= SW_ORING, "offsets ring holds a tile's window");
-static_assert(SW_EMAX == 64, "each lane holds two of a tile's segment ends");
+static_assert((SW_EMAXT + 1) * 8 + SW_OCHUNK <= SW_ORING, "offsets ring holds a tile's window");
+static_assert(SW_EMAXT % 32 == 0, "ends are taken 32 at a time");
 
 // Per-warp shared memory.
 struct WarpSmem {
     static constexpr uint32_t vstage = 0;
     static constexpr uint32_t oring = SW_NSV * SW_VCHUNK;
-    static constexpr uint32_t marks = oring + SW_ORING;
-    static constexpr uint32_t argr = marks + 32 * 4;
+    static constexpr uint32_t xs = oring + SW_ORING;        // [32] lane prefix values
+    static constexpr uint32_t xr = xs + 32 * 4;             // [32] lane prefix rows
+    static constexpr uint32_t argr = xr + 32 * 4;           // [SW_TROWS] int16; start flags
     static constexpr uint32_t bars = argr + SW_TROWS * 2;
-    static constexpr uint32_t bytes = ((bars + (SW_NSV + SW_NSO) * 8 + 1023) / 1024) * 1024;
+    static constexpr uint32_t bytes = ((bars + (SW_NSV + SW_NSO) * 8 + 127) / 128) * 128;
 };
 constexpr uint32_t SW_SMEM = SW_NW * WarpSmem::bytes;
+static_assert(SW_SMEM <= 227 * 1024, "one CTA per SM");
 
 // Search scratch (aliases the warps' memory before they start).
 struct SearchSmem {
     int64_t graw[SW_GRID];
-    int64_t D[SW_NDIAG], lo[SW_NDIAG], hi[SW_NDIAG];
+    int64_t D[SW_NDIAG], lo[SW_NDIAG], hi[SW_NDIAG], R[SW_NDIAG];
     int cnt[SW_NDIAG];
     int64_t o0, oS;
 };
@@ -118,9 +129,11 @@ __device__ __forceinline__ void warp_combine_store(const Params& p, const PartEl
 template <class T, int OP, class OffT>
 __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params p) {
     using RD = Red<T, OP>;
-    using CO = Carry<T, OP>;
+    using CO = ScalarCarry<T, OP>;
     using C = typename CO::C;
     constexpr uint32_t OSZ = sizeof(OffT);
+    constexpr bool kFloatSum = OP == OP_SUM && kIsFloat<T>;
+    constexpr unsigned FULL = 0xffffffffu;
 
     extern __shared__ __align__(1024) unsigned char smem[];
     const int tid = threadIdx.x;
@@ -133,9 +146,11 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     const int64_t U = static_cast<int64_t>(p.P) * SW_NW;   // units in the grid
 
     // ---- a2: unit boundaries ---------------------------------------------------
-    // I(D) = #{s : key(s) < D}, key(s) = (offsets[s+1] - o0) + s.  Round 1
-    // reads a fixed grid of SW_GRID keys that every CTA shares (so it hits L2);
-    // then each boundary narrows its bracket with SW_PROBES probes per round.
+    // Weighted merge path: end s sits at key(s) = (offsets[s+1] - o0) + SW_CW s.
+    // A cut at D takes the I(D) = #{s : key(s) < D} ends before it and the rows
+    // before both D - SW_CW I and the start of segment I.  Round 1 reads a
+    // fixed grid of SW_GRID keys that every CTA shares (so it hits L2); then
+    // each boundary narrows its bracket with SW_PROBES probes per round.
     SearchSmem* ss = reinterpret_cast<SearchSmem*>(smem);
     if (tid == 0) ss->o0 = clamp_off(__ldg(&offs[0]), N);
     if (tid == 1) ss->oS = clamp_off(__ldg(&offs[S]), N);
@@ -147,18 +162,19 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     const int64_t o0 = ss->o0;
     const int64_t oS = ss->oS < o0 ? o0 : ss->oS;
     const int64_t nrows = oS - o0;
-    const int64_t total = nrows + S;
+    const int64_t total = nrows + SW_CW * S;
     const int64_t Wu = (total + U - 1) / U;
     if (tid < SW_NDIAG) {
         const int64_t u = static_cast<int64_t>(cta) * SW_NW + tid;
         const int64_t D = u * Wu < total ? u * Wu : total;
-        int64_t lo = D - nrows > 0 ? D - nrows : 0;
-        int64_t hi = D < S ? D : S;
+        int64_t lo = D > nrows ? (D - nrows + SW_CW - 1) / SW_CW : 0;
+        int64_t hi = (D + SW_CW - 1) / SW_CW;
+        hi = hi < S ? hi : S;
         int a = 0, b = SW_GRID;   // c = #{m : key(s_m) < D}
         while (a < b) {
             const int mid = (a + b) >> 1;
             const int64_t sm = static_cast<int64_t>(mid) * S / SW_GRID;
-            if (ss->graw[mid] - o0 + sm < D)
+            if (ss->graw[mid] - o0 + SW_CW * sm < D)
                 a = mid + 1;
             else
                 b = mid;
@@ -186,7 +202,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
                 if (len > 0) {
                     const int64_t step = (len + SW_PROBES - 1) / SW_PROBES;
                     const int64_t s = lo + mm * step;
-                    if (s < hi && clamp_off(__ldg(&offs[s + 1]), N) - o0 + s < ss->D[k])
+                    if (s < hi && clamp_off(__ldg(&offs[s + 1]), N) - o0 + SW_CW * s < ss->D[k])
                         atomicAdd(&ss->cnt[k], 1);
                 }
             }
@@ -214,15 +230,23 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
         }
         if (!__syncthreads_or(open)) break;
     }
-    // my unit: merge positions [D_w, D_w+1), ends [Iu, Iu2), rows [Ru, Ru2)
+    if (tid < SW_NDIAG) {
+        // rows before the cut: D - SW_CW I, but never fewer than segment I's start
+        const int64_t I = ss->lo[tid];
+        const int64_t oI = I > 0 ? clamp_off(__ldg(&offs[I]), N) - o0 : 0;
+        int64_t R = ss->D[tid] - SW_CW * I;
+        R = R < oI ? oI : R;
+        R = R < 0 ? 0 : (R > nrows ? nrows : R);
+        ss->R[tid] = o0 + R;
+    }
+    __syncthreads();
+    // my unit: weighted positions [Dlo, Dhi), ends [Iu, Iu2), rows [Ru, Ru2)
     const int64_t u_me = static_cast<int64_t>(cta) * SW_NW + warp;
     const int64_t Dlo = ss->D[warp], Dhi = ss->D[warp + 1];
     const int64_t Iu = ss->lo[warp];
     const int64_t Iu2 = ss->lo[warp + 1] > Iu ? ss->lo[warp + 1] : Iu;
-    int64_t Ru = Dlo - Iu + o0;
-    Ru = Ru < o0 ? o0 : (Ru > oS ? oS : Ru);
-    int64_t Ru2 = Dhi - Iu2 + o0;
-    Ru2 = Ru2 < Ru ? Ru : (Ru2 > oS ? oS : Ru2);
+    const int64_t Ru = ss->R[warp];
+    const int64_t Ru2 = ss->R[warp + 1] > Ru ? ss->R[warp + 1] : Ru;
     __syncthreads();   // the search scratch is dead from here on
     if (Dlo >= Dhi) return;
 
@@ -230,8 +254,12 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     unsigned char* wbase = smem + warp * WarpSmem::bytes;
     unsigned char* vst = wbase + WarpSmem::vstage;
     unsigned char* oring = wbase + WarpSmem::oring;
-    uint32_t* marks = reinterpret_cast<uint32_t*>(wbase + WarpSmem::marks);
+    uint32_t* xs = reinterpret_cast<uint32_t*>(wbase + WarpSmem::xs);
+    int32_t* xr = reinterpret_cast<int32_t*>(wbase + WarpSmem::xr);
     int16_t* argr = reinterpret_cast<int16_t*>(wbase + WarpSmem::argr);
+    // Start flags (one byte per chunk row) share argr's bytes: a tile reads
+    // them before it writes argr, and clears them once it is done with argr.
+    unsigned char* flg = wbase + WarpSmem::argr;
     uint64_t* fv = reinterpret_cast<uint64_t*>(wbase + WarpSmem::bars);
     uint64_t* fo = fv + SW_NSV;
     T* out = static_cast<T*>(p.out);
@@ -246,44 +274,73 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
                                   SW_VCHUNK);
     const Stream os = make_stream(obase, static_cast<uint64_t>(S + 1) * OSZ, obase + Iu * OSZ,
                                   obase + (Iu2 + 1) * OSZ, SW_OCHUNK);
-    const int64_t vrow0 = static_cast<int64_t>(vs.A0 - vbase) / 4;   // row of chunk 0's first byte
+    const int32_t nR = static_cast<int32_t>(Ru2 - Ru);
+    // chunk 0's first row, relative to Ru (in [-3, 0]: chunks start 16-byte aligned)
+    const int32_t cb0 = static_cast<int32_t>(static_cast<int64_t>(vs.A0 - vbase) / 4 - Ru);
     const uint64_t policy = policy_evict_first();
+    // ring byte of offsets entry Iu + i is (o_at0 + i * OSZ) mod SW_ORING
+    const uint32_t o_at0 = static_cast<uint32_t>(obase + static_cast<uint64_t>(Iu) * OSZ - os.A0);
 
-    marks[lane] = 0u;
+    // Value chunk k into its stage (lane 0).  Chunks inside the buffer's
+    // 16-byte-aligned interior take one bulk copy; the first and last may
+    // need plain loads for their edges.
+    auto issue_v = [&](int64_t k) {
+        unsigned char* dst = vst + (k % SW_NSV) * SW_VCHUNK;
+        uint64_t* bar = &fv[k % SW_NSV];
+        const uint64_t cs = vs.A0 + static_cast<uint64_t>(k) * SW_VCHUNK;
+        if (cs >= vs.TA && cs + SW_VCHUNK <= vs.TE && cs + SW_VCHUNK <= vs.AE) {
+            mbar_arrive_expect_tx(bar, SW_VCHUNK);
+            bulk_load(dst, reinterpret_cast<const void*>(cs), SW_VCHUNK, bar, policy);
+        } else {
+            issue_chunk_to(vs, k, SW_VCHUNK, dst, bar, policy);
+        }
+    };
+    // L2 prefetch of the interior bytes of value chunk k (lane 0)
+    auto prefetch_v = [&](int64_t k) {
+        if (k >= vs.nch) return;
+        const uint64_t cs = vs.A0 + static_cast<uint64_t>(k) * SW_VCHUNK;
+        uint64_t ce = cs + SW_VCHUNK;
+        ce = ce < vs.AE ? ce : vs.AE;
+        ce = ce < vs.TE ? ce : vs.TE;
+        const uint64_t c0 = cs > vs.TA ? cs : vs.TA;
+        if (ce > c0) bulk_prefetch_l2(reinterpret_cast<const void*>(c0), static_cast<uint32_t>(ce - c0));
+    };
+    constexpr int kPrefetch = 2;   // value chunks prefetched into L2 beyond the staged ones
+
     if (lane == 0) {
         for (int k = 0; k < SW_NSV + SW_NSO; ++k) mbar_init(&fv[k], 1);
         fence_mbarrier_init();
     }
+    // clear my flag bytes
+#pragma unroll
+    for (int q = 0; q < SW_Q; ++q) reinterpret_cast<uint32_t*>(flg + lane * SW_KR)[q] = 0u;
     __syncwarp();
-    int64_t v_issued = 0, o_issued = 0;       // lane 0's counters (kept uniform by shuffles)
+    // counters below are kept identical in every lane; lane 0 issues the copies
+    int64_t v_issued = SW_NSV < vs.nch ? SW_NSV : vs.nch;
+    int64_t o_issued = SW_NSO < os.nch ? SW_NSO : os.nch;
     if (lane == 0) {
-        for (; v_issued < SW_NSV && v_issued < vs.nch; ++v_issued)
-            issue_chunk_to(vs, v_issued, SW_VCHUNK, vst + (v_issued % SW_NSV) * SW_VCHUNK,
-                           &fv[v_issued % SW_NSV], policy);
-        for (; o_issued < SW_NSO && o_issued < os.nch; ++o_issued)
-            issue_chunk(os, o_issued, oring, SW_ORING, SW_OCHUNK, &fo[o_issued % SW_NSO], policy);
+        for (int64_t k = 0; k < v_issued; ++k) issue_v(k);
+        for (int k = 0; k < kPrefetch; ++k) prefetch_v(v_issued + k);
+        for (int64_t k = 0; k < o_issued; ++k)
+            issue_chunk(os, k, oring, SW_ORING, SW_OCHUNK, &fo[k % SW_NSO], policy);
     }
 
-    auto off_w = [&](int64_t s) -> int64_t {
-        const uint32_t at = static_cast<uint32_t>((obase + static_cast<uint64_t>(s) * OSZ) - os.A0) &
-                            (SW_ORING - 1);
-        return clamp_off(*reinterpret_cast<const OffT*>(oring + at), N);
+    // offsets[Iu + i] from the ring, as a row relative to Ru clamped to
+    // [-1, nR + 1] (which also keeps malformed offsets inside the unit)
+    auto off_rel = [&](int64_t i) -> int32_t {
+        const uint32_t at = (o_at0 + static_cast<uint32_t>(i) * OSZ) & (SW_ORING - 1);
+        const int64_t x = static_cast<int64_t>(*reinterpret_cast<const OffT*>(oring + at)) - Ru;
+        return static_cast<int32_t>(x < -1 ? -1 : (x > nR + 1 ? nR + 1 : x));
     };
     int64_t ow = 0, odone = 0;   // offsets chunks waited for / handed back
     bool ok = true;
-    // wait until offsets entry x is in the ring (uniform across the warp)
-    auto wait_offsets = [&](int64_t x) {
-        const int64_t need =
-            static_cast<int64_t>((obase + static_cast<uint64_t>(x + 1) * OSZ - 1 - os.A0) / SW_OCHUNK);
-        if (ow <= need && ow < os.nch) {
-            if (lane == 0)
-                for (; ok && ow <= need && ow < os.nch; ++ow)
-                    ok = wait_bounded(&fo[ow % SW_NSO], static_cast<uint32_t>((ow / SW_NSO) & 1), p.status,
-                                      STATUS_CONSUMER_TIMEOUT);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            ow = __shfl_sync(0xffffffffu, ow, 0);
-            __syncwarp();
-        }
+    // wait until offsets entry Iu + i is in the ring
+    auto wait_offsets = [&](int64_t i) {
+        const int64_t need = static_cast<int64_t>((o_at0 + static_cast<uint64_t>(i + 1) * OSZ - 1) / SW_OCHUNK);
+        for (; ok && ow <= need && ow < os.nch; ++ow)
+            ok = wait_bounded(&fo[ow % SW_NSO], static_cast<uint32_t>((ow / SW_NSO) & 1), p.status,
+                              STATUS_CONSUMER_TIMEOUT);
+        ok = __all_sync(FULL, ok);
     };
 
     C carry = CO::ident();
@@ -291,282 +348,329 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     bool head_pending = (Iu < S) && off_Iu < Ru;
     int64_t m = 0;            // current value chunk
     bool m_ready = false;
-    int64_t es = Iu;          // next segment end
-    int64_t b_es = off_Iu;    // offsets[es]
-    int64_t j = Ru;           // next row
+    int32_t ie = 0;           // next segment end, relative to Iu
+    const int32_t nE = static_cast<int32_t>(Iu2 - Iu);
+    int32_t b_es = off_Iu - Ru < -1 ? -1 : static_cast<int32_t>(off_Iu - Ru);   // offsets[Iu + ie]
+    int32_t jj = 0;           // next row
 
     while (ok) {
         const bool lastc = m + 1 >= vs.nch;
-        const int64_t crow0 = vrow0 + m * SW_TROWS;
-        const int64_t rl = lastc ? Ru2 : (crow0 + SW_TROWS < Ru2 ? crow0 + SW_TROWS : Ru2);
+        const int32_t cb = cb0 + static_cast<int32_t>(m) * SW_TROWS;   // chunk m's first row
+        const int32_t rl = lastc ? nR : (cb + SW_TROWS < nR ? cb + SW_TROWS : nR);
         if (m < vs.nch && !m_ready) {
-            if (lane == 0)
-                ok = wait_bounded(&fv[m % SW_NSV], static_cast<uint32_t>((m / SW_NSV) & 1), p.status,
-                                  STATUS_CONSUMER_TIMEOUT);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            __syncwarp();
+            ok = __all_sync(FULL, wait_bounded(&fv[m % SW_NSV], static_cast<uint32_t>((m / SW_NSV) & 1),
+                                               p.status, STATUS_CONSUMER_TIMEOUT));
             m_ready = true;
             if (!ok) break;
         }
-        const int64_t rem = Iu2 - es;
-        const int ncand = static_cast<int>(rem < SW_EMAX ? rem : SW_EMAX);
-        wait_offsets(es + ncand);
-        if (!ok) break;
-        // Lane l holds ends es + l and es + 32 + l: E = offsets[s + 1] (the
-        // segment's end, which is the next segment's start), B = offsets[s].
-        int64_t E[2], B[2];
-        bool have[2];
+        const int32_t rem = nE - ie;
+        const int ncand = rem < SW_EMAXT ? rem : SW_EMAXT;
+        if (ncand > 0) {
+            wait_offsets(ie + ncand);
+            if (!ok) break;
+        }
+        // This tile's ends: the prefix of the candidates whose segment ends by
+        // row rl (all of them on the unit's last chunk).  Lane l keeps
+        // E[g] = offsets[s + 1] of end s = Iu + ie + 32 g + l.
+        constexpr int NG = SW_EMAXT / 32;
+        int32_t E[NG];
+        int n_e = 0;
+        bool more = true;
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int idx = 32 * k + lane;
-            have[k] = idx < ncand;
-            E[k] = have[k] ? off_w(es + idx + 1) : INT64_MAX;
-        }
-        {
-            const int64_t up0 = __shfl_up_sync(0xffffffffu, E[0], 1);
-            const int64_t up1 = __shfl_up_sync(0xffffffffu, E[1], 1);
-            const int64_t last0 = __shfl_sync(0xffffffffu, E[0], 31);
-            B[0] = lane == 0 ? b_es : up0;
-            B[1] = lane == 0 ? last0 : up1;
-        }
-        // ends of this tile: a prefix of those whose segment ends by row rl
-        // (all of them on the unit's last chunk)
-        int n_e = ncand;
-        if (!lastc) {
-            const unsigned b0 = __ballot_sync(0xffffffffu, have[0] && E[0] <= rl);
-            int run = b0 == 0xffffffffu ? 32 : __ffs(~b0) - 1;
-            if (run == 32) {
-                const unsigned b1 = __ballot_sync(0xffffffffu, have[1] && E[1] <= rl);
-                run += b1 == 0xffffffffu ? 32 : __ffs(~b1) - 1;
+        for (int g = 0; g < NG; ++g) {
+            E[g] = INT32_MAX;
+            if (more && 32 * g < ncand) {
+                const int idx = 32 * g + lane;
+                if (idx < ncand) E[g] = off_rel(ie + idx + 1);
+                const unsigned b = __ballot_sync(FULL, idx < ncand && (lastc || E[g] <= rl));
+                if (b != FULL) {
+                    n_e += __ffs(~b) - 1;
+                    more = false;
+                } else {
+                    n_e += 32;
+                }
             }
-            n_e = run < ncand ? run : ncand;
         }
-        int64_t tr1 = rl;
-        if (n_e == SW_EMAX && es + n_e < Iu2) {
-            const int64_t x = __shfl_sync(0xffffffffu, E[1], 31);   // rows up to the last included end
-            tr1 = x < j ? j : (x > rl ? rl : x);
-        }
-        if (n_e == 0 && j >= tr1) {
-            // nothing left in this chunk
-            if (lastc) break;
+        n_e = n_e < ncand ? n_e : ncand;
+        const bool capped = n_e == SW_EMAXT && ie + n_e < nE;
+        // the segment left open after this tile starts at offsets[Iu + ie + n_e],
+        // the E of the tile's last end
+        int32_t elast = b_es;
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+            if (((n_e - 1) >> 5) == g) elast = E[g];
+        const int32_t bo = n_e == 0 ? b_es : __shfl_sync(FULL, elast, (n_e - 1) & 31);
+        const int32_t tr1 = capped ? (bo < jj ? jj : (bo > rl ? rl : bo)) : rl;
+
+        // ---- one tile: rows [jj, tr1) of chunk m, ends [ie, ie + n_e) ---------------
+        if (n_e > 0 || jj < tr1) {
+            unsigned char* stage = vst + (m % SW_NSV) * SW_VCHUNK;
+            const int32_t jr = jj - cb;       // rows relative to the chunk
+            const int32_t tr = tr1 - cb;
+            const bool has_rows = tr1 > jj && m < vs.nch;
+            const int32_t lrow0 = lane * SW_KR;   // my first row, relative to the chunk
+            unsigned char* mine = stage + lane * (SW_KR * 4);
+            if (has_rows && n_e == 0 && jr == 0 && tr == SW_TROWS) {
+                // The whole chunk lies inside one segment: fold it.
+                Acc<T> a = RD::ident();
+#pragma unroll
+                for (int q = 0; q < SW_Q; ++q) {
+                    const uint4 u4 = *reinterpret_cast<const uint4*>(mine + 16 * q);
+                    if constexpr (OP == OP_SUM) {
+                        const T s01 = add_wrap(from_bits<T>(u4.x), from_bits<T>(u4.y));
+                        const T s23 = add_wrap(from_bits<T>(u4.z), from_bits<T>(u4.w));
+                        a.v = add_wrap(a.v, add_wrap(s01, s23));
+                    } else {
+                        const uint32_t xb[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) RD::add(a, from_bits<T>(xb[t]), lrow0 + 4 * q + t);
+                    }
+                }
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    Acc<T> b;
+                    b.v = from_bits<T>(__shfl_xor_sync(FULL, bits_of(a.v), o));
+                    b.row = OP == OP_SUM ? -1 : __shfl_xor_sync(FULL, a.row, o);
+                    a = (lane & o) ? RD::comb(b, a) : RD::comb(a, b);
+                }
+                if constexpr (OP != OP_SUM) a.row += cb;
+                carry = b_es < jj ? CO::then(carry, a) : CO::from(a);
+            } else {
+                if (has_rows) {
+                    // start flags: the tile's first row and, for each end, the
+                    // row where the next segment starts
+                    if (lane == 0) flg[jr] = 1;
+#pragma unroll
+                    for (int g = 0; g < NG; ++g) {
+                        if (32 * g + lane < n_e && E[g] >= jj && E[g] < tr1) flg[E[g] - cb] = 1;
+                    }
+                    __syncwarp();
+                    uint32_t fw[SW_Q];
+#pragma unroll
+                    for (int q = 0; q < SW_Q; ++q) fw[q] = reinterpret_cast<const uint32_t*>(flg + lane * SW_KR)[q];
+                    __syncwarp();
+                    if constexpr (OP == OP_SUM) {
+                        // sum writes no argr: clear my flags at once
+#pragma unroll
+                        for (int q = 0; q < SW_Q; ++q) reinterpret_cast<uint32_t*>(flg + lane * SW_KR)[q] = 0u;
+                    }
+                    // inclusive segmented scan of my rows, a quad at a time
+                    const int32_t hi = tr - lrow0;        // my rows below tr1
+                    Acc<T> acc = RD::ident();
+                    bool fi = false;
+#pragma unroll
+                    for (int q = 0; q < SW_Q; ++q) {
+                        const uint4 u4 = *reinterpret_cast<const uint4*>(mine + 16 * q);
+                        uint32_t xb[4] = {u4.x, u4.y, u4.z, u4.w};
+                        int16_t rr[4];
+                        fi = fi || fw[q] != 0u;
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int k = 4 * q + t;
+                            const T x = from_bits<T>(xb[t]);
+                            const bool reset = (fw[q] >> (8 * t)) & 1u;
+                            if constexpr (OP == OP_SUM) {
+                                acc.v = reset ? x : add_wrap(acc.v, x);
+                            } else {
+                                const bool better = (OP == OP_MIN) ? (x < acc.v) : (x > acc.v);
+                                if (reset || acc.row < 0 || better) {
+                                    acc.v = x;
+                                    acc.row = lrow0 + k;
+                                }
+                                rr[t] = static_cast<int16_t>(acc.row);
+                            }
+                            xb[t] = bits_of(acc.v);
+                        }
+                        // running values back over rows < tr1 (later rows are the
+                        // next tile's input; earlier rows are finished)
+                        if (4 * q + 4 <= hi) {
+                            *reinterpret_cast<uint4*>(mine + 16 * q) = make_uint4(xb[0], xb[1], xb[2], xb[3]);
+                            if constexpr (OP != OP_SUM)
+                                *reinterpret_cast<uint2*>(&argr[lrow0 + 4 * q]) = make_uint2(
+                                    (static_cast<uint32_t>(static_cast<uint16_t>(rr[1])) << 16) |
+                                        static_cast<uint16_t>(rr[0]),
+                                    (static_cast<uint32_t>(static_cast<uint16_t>(rr[3])) << 16) |
+                                        static_cast<uint16_t>(rr[2]));
+                        } else if (4 * q < hi) {
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                if (4 * q + t < hi) {
+                                    *reinterpret_cast<uint32_t*>(mine + 16 * q + 4 * t) = xb[t];
+                                    if constexpr (OP != OP_SUM) argr[lrow0 + 4 * q + t] = rr[t];
+                                }
+                            }
+                        }
+                    }
+                    // segmented scan of the lane totals; the exclusive prefix of
+                    // each lane goes to shared memory
+                    Acc<T> inc = acc;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        Acc<T> pv;
+                        pv.v = from_bits<T>(__shfl_up_sync(FULL, bits_of(inc.v), o));
+                        if constexpr (OP != OP_SUM) pv.row = __shfl_up_sync(FULL, inc.row, o);
+                        else pv.row = -1;
+                        const bool pf = __shfl_up_sync(FULL, fi, o);
+                        if (lane >= o) {
+                            if (!fi) inc = RD::comb(pv, inc);
+                            fi = fi || pf;
+                        }
+                    }
+                    const uint32_t xv = __shfl_up_sync(FULL, bits_of(inc.v), 1);
+                    xs[lane] = xv;
+                    if constexpr (OP != OP_SUM) {
+                        const int32_t xrow = __shfl_up_sync(FULL, inc.row, 1);
+                        xr[lane] = lane == 0 ? -1 : xrow;
+                    }
+                    __syncwarp();
+                }
+                // Running value at chunk row k (jr <= k < tr) of the run that
+                // starts at chunk row st: the stored running value, joined with
+                // the owning lane's prefix when the run began in an earlier
+                // lane.  min / max rows come back relative to Ru.
+                auto running_at = [&](int32_t k, int32_t st) -> Acc<T> {
+                    if (!has_rows) return RD::ident();
+                    k = k < jr ? jr : (k >= tr ? tr - 1 : k);
+                    const int o = k / SW_KR;
+                    Acc<T> P;
+                    P.v = *reinterpret_cast<const T*>(stage + k * 4);
+                    P.row = OP == OP_SUM ? -1 : static_cast<int32_t>(argr[k]) + cb;
+                    if (st < o * SW_KR) {
+                        Acc<T> Xo;
+                        Xo.v = from_bits<T>(xs[o]);
+                        Xo.row = -1;
+                        if constexpr (OP != OP_SUM) {
+                            const int32_t r = xr[o];
+                            Xo.row = r < 0 ? -1 : r + cb;
+                        }
+                        P = RD::comb(Xo, P);
+                    }
+                    return P;
+                };
+                bool skip_first = false;
+                if (head_pending && n_e > 0) {
+                    // end Iu began in an earlier unit: leave the head partial and
+                    // join the ticket (the whole warp takes part)
+                    const int32_t oe = __shfl_sync(FULL, E[0], 0);
+                    const bool rows_here = has_rows && oe - 1 >= jj;
+                    const Acc<T> P = running_at(oe - 1 - cb, jr);
+                    const C R = rows_here ? CO::then(carry, P) : carry;
+                    bool last = false;
+                    int pc = 0;
+                    if (lane == 0) {
+                        if constexpr (kFloatSum) heads[u_me] = to_part(R);
+                        else heads[u_me] = to_part<T, OP>(R, Ru);
+                        __threadfence();
+                        pc = static_cast<int>((off_Iu - o0 + SW_CW * Iu) / Wu);
+                        pc = pc < 0 ? 0 : (pc > u_me ? static_cast<int>(u_me) : pc);
+                        last = ticket_arrive(p.ws_tickets, static_cast<int>(u_me),
+                                             static_cast<int>(u_me) - pc + 1, p.gen);
+                        if (last) __threadfence();
+                    }
+                    last = __shfl_sync(FULL, last, 0);
+                    pc = __shfl_sync(FULL, pc, 0);
+                    if (last) {
+                        const int64_t oe1 = clamp_off(__ldg(&offs[Iu + 1]), N);
+                        warp_combine_store<T, OP>(p, tails, heads, pc, static_cast<int>(u_me), Iu,
+                                                  oe1 > off_Iu ? oe1 - off_Iu : 0, lane);
+                    }
+                    skip_first = true;   // lane 0 of the first group skips end Iu below
+                }
+                // the ends, 32 at a time: E = offsets[s + 1], B = offsets[s]
+                int32_t prevE = b_es;
+#pragma unroll
+                for (int g = 0; g < NG; ++g) {
+                    if (32 * g < n_e) {
+                        const int idx = 32 * g + lane;
+                        const bool valid = idx < n_e && !(g == 0 && lane == 0 && skip_first);
+                        const int32_t oe = E[g];
+                        const int32_t up = __shfl_up_sync(FULL, oe, 1);
+                        const int32_t ob = lane == 0 ? prevE : up;
+                        prevE = __shfl_sync(FULL, oe, 31);
+                        if (valid) {
+                            const int64_t s = Iu + ie + idx;
+                            const int32_t len = oe > ob ? oe - ob : 0;
+                            T v;
+                            int64_t a;
+                            if (len == 0) {
+                                v = T(0);
+                                a = -1;
+                            } else if (ob >= jj) {
+                                finish_acc<T, OP>(running_at(oe - 1 - cb, ob - cb), len, mean, Ru, v, a);
+                            } else {
+                                const bool rows_here = has_rows && oe - 1 >= jj;
+                                const C R = rows_here ? CO::then(carry, running_at(oe - 1 - cb, jr)) : carry;
+                                if constexpr (kFloatSum) {
+                                    finish_carry(R, len, mean, v);
+                                    a = -1;
+                                } else {
+                                    finish_acc<T, OP>(R, len, mean, Ru, v, a);
+                                }
+                            }
+                            out[s] = v;
+                            if (want_arg) p.out_arg[s] = a;
+                        }
+                    }
+                }
+                // carry of the segment left open, which starts at bo
+                const int32_t sto = bo > jj ? bo : jj;
+                if (has_rows && sto < tr1) {
+                    const Acc<T> P = running_at(tr - 1, sto - cb);
+                    carry = bo < jj ? CO::then(carry, P) : CO::from(P);
+                } else if (!(bo < jj)) {
+                    carry = CO::ident();
+                }
+                if constexpr (OP != OP_SUM) {
+                    if (has_rows) {
+                        // done with argr: clear my flag bytes for the next tile
+                        __syncwarp();
+#pragma unroll
+                        for (int q = 0; q < SW_Q; ++q) reinterpret_cast<uint32_t*>(flg + lane * SW_KR)[q] = 0u;
+                    }
+                }
+            }
+            if (n_e > 0) head_pending = false;
+            b_es = bo;
+            jj = tr1;
+            ie += n_e;
             __syncwarp();
-            if (lane == 0 && v_issued < vs.nch) {
-                issue_chunk_to(vs, v_issued, SW_VCHUNK, vst + (v_issued % SW_NSV) * SW_VCHUNK,
-                               &fv[v_issued % SW_NSV], policy);
+            // hand back offsets chunks that hold only entries before Iu + ie
+            const int64_t keep_from = static_cast<int64_t>((o_at0 + static_cast<uint64_t>(ie) * OSZ) / SW_OCHUNK);
+            if (odone < keep_from && odone < ow) {
+                const int64_t upto = keep_from < ow ? keep_from : ow;
+                if (lane == 0) {
+                    for (int64_t k = odone; k < upto; ++k) {
+                        const int64_t nk = k + SW_NSO;
+                        if (nk < os.nch)
+                            issue_chunk(os, nk, oring, SW_ORING, SW_OCHUNK, &fo[nk % SW_NSO], policy);
+                    }
+                }
+                o_issued = upto + SW_NSO < os.nch ? upto + SW_NSO : os.nch;
+                odone = upto;
+            }
+        }
+        // The chunk is finished once its rows are done and no further end
+        // falls in it (the tile was not cut short by the ends cap).
+        if (jj >= rl && !capped) {
+            if (lastc) {
+                if (ie >= nE) break;
+                continue;   // malformed offsets only: drain the remaining ends
+            }
+            // the stage is refilled by the async proxy: order this warp's
+            // reads and write-backs of it first
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (v_issued < vs.nch) {
+                if (lane == 0) {
+                    issue_v(v_issued);
+                    prefetch_v(v_issued + kPrefetch);
+                }
                 ++v_issued;
             }
             ++m;
             m_ready = false;
-            continue;
         }
-
-        // ---- one tile: rows [j, tr1) of chunk m, ends [es, es + n_e) ----------------
-        unsigned char* stage = vst + (m % SW_NSV) * SW_VCHUNK;
-        const int32_t jr = static_cast<int32_t>(j - crow0);       // rows relative to the chunk
-        const int32_t tr = static_cast<int32_t>(tr1 - crow0);
-        const bool has_rows = tr1 > j && m < vs.nch;
-        const int32_t crow_u = static_cast<int32_t>(crow0 - Ru);  // chunk row 0, relative to the unit
-        Acc<T> X = RD::ident();   // running value of the rows before my lane's rows
-        if (has_rows) {
-            // 1. marks: the segment after each of this tile's ends starts at its E
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                if (32 * k + lane < n_e && E[k] >= j && E[k] < tr1) {
-                    const int32_t rr = static_cast<int32_t>(E[k] - crow0);
-                    atomicOr(&marks[rr / SW_KR], 1u << (rr % SW_KR));
-                }
-            }
-            if (lane == 0) atomicOr(&marks[jr / SW_KR], 1u << (jr % SW_KR));
-            __syncwarp();
-            // 2. rows
-            const uint32_t w = marks[lane];
-            marks[lane] = 0u;
-            uint32_t xb[SW_KR];
-#pragma unroll
-            for (int q = 0; q < SW_KR / 4; ++q) {
-                const uint4 u4 = *reinterpret_cast<const uint4*>(stage + lane * (SW_KR * 4) + 16 * q);
-                xb[4 * q + 0] = u4.x;
-                xb[4 * q + 1] = u4.y;
-                xb[4 * q + 2] = u4.z;
-                xb[4 * q + 3] = u4.w;
-            }
-            const int32_t lrow0 = lane * SW_KR;              // my first row, relative to the chunk
-            Acc<T> acc = RD::ident();
-            int16_t rr[OP == OP_SUM ? 1 : SW_KR];
-#pragma unroll
-            for (int k = 0; k < SW_KR; ++k) {
-                const T x = from_bits<T>(xb[k]);
-                const bool reset = (w >> k) & 1u;
-                if constexpr (OP == OP_SUM) {
-                    acc.v = reset ? x : add_wrap(acc.v, x);
-                } else {
-                    const bool better = (OP == OP_MIN) ? (x < acc.v) : (x > acc.v);
-                    if (reset || acc.row < 0 || better) {
-                        acc.v = x;
-                        acc.row = crow_u + lrow0 + k;
-                    }
-                    rr[k] = static_cast<int16_t>(acc.row - crow_u);
-                }
-                xb[k] = bits_of(acc.v);
-            }
-            // write the running values back over rows < tr1 (later rows are the
-            // next tile's input; earlier rows are finished)
-            const int32_t hi = tr - lrow0;
-            if (hi >= SW_KR) {
-#pragma unroll
-                for (int q = 0; q < SW_KR / 4; ++q)
-                    *reinterpret_cast<uint4*>(stage + lane * (SW_KR * 4) + 16 * q) =
-                        make_uint4(xb[4 * q], xb[4 * q + 1], xb[4 * q + 2], xb[4 * q + 3]);
-                if constexpr (OP != OP_SUM) {
-#pragma unroll
-                    for (int q = 0; q < SW_KR / 2; ++q)
-                        *reinterpret_cast<uint32_t*>(&argr[lrow0 + 2 * q]) =
-                            (static_cast<uint32_t>(static_cast<uint16_t>(rr[2 * q + 1])) << 16) |
-                            static_cast<uint16_t>(rr[2 * q]);
-                }
-            } else if (hi > 0) {
-#pragma unroll
-                for (int k = 0; k < SW_KR; ++k) {
-                    if (k < hi) {
-                        *reinterpret_cast<uint32_t*>(stage + (lrow0 + k) * 4) = xb[k];
-                        if constexpr (OP != OP_SUM) argr[lrow0 + k] = rr[k];
-                    }
-                }
-            }
-            // segmented scan of the lane totals; X = exclusive prefix
-            Acc<T> inc = acc;
-            bool fi = w != 0u;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                Acc<T> pv;
-                pv.v = from_bits<T>(__shfl_up_sync(0xffffffffu, bits_of(inc.v), o));
-                if constexpr (OP != OP_SUM) pv.row = __shfl_up_sync(0xffffffffu, inc.row, o);
-                else pv.row = -1;
-                const bool pf = __shfl_up_sync(0xffffffffu, fi, o);
-                if (lane >= o) {
-                    if (!fi) inc = RD::comb(pv, inc);
-                    fi = fi || pf;
-                }
-            }
-            X.v = from_bits<T>(__shfl_up_sync(0xffffffffu, bits_of(inc.v), 1));
-            if constexpr (OP != OP_SUM) X.row = __shfl_up_sync(0xffffffffu, inc.row, 1);
-            if (lane == 0) X = RD::ident();
-            __syncwarp();
-        }
-        // running value at chunk row `k` (jr <= k < tr) of the run starting at
-        // chunk row `st`: the lane's running value there, joined with the owning
-        // lane's prefix when the run began in an earlier lane (every lane calls
-        // this together: it shuffles)
-        auto running_at = [&](int32_t k, int32_t st) -> Acc<T> {
-            if (!has_rows) return RD::ident();   // uniform across the warp
-            k = k < jr ? jr : (k >= tr ? tr - 1 : k);
-            const int o = k / SW_KR;
-            Acc<T> Xo;
-            Xo.v = from_bits<T>(__shfl_sync(0xffffffffu, bits_of(X.v), o));
-            if constexpr (OP != OP_SUM) Xo.row = __shfl_sync(0xffffffffu, X.row, o);
-            else Xo.row = -1;
-            Acc<T> P;
-            P.v = *reinterpret_cast<const T*>(stage + k * 4);
-            if constexpr (OP == OP_SUM) {
-                P.row = -1;
-            } else {
-                P.row = static_cast<int32_t>(argr[k]) + crow_u;
-            }
-            return st < o * SW_KR ? RD::comb(Xo, P) : P;
-        };
-        // 3. ends
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            if (k == 1 && n_e <= 32) break;
-            const int idx = 32 * k + lane;
-            const bool valid = idx < n_e;
-            const int64_t s = es + idx;
-            const int64_t ob = valid ? B[k] : j;
-            const int64_t oe = valid ? E[k] : j;
-            const bool rows_here = valid && has_rows && oe > ob && oe - 1 >= j;
-            const int32_t kl = rows_here ? static_cast<int32_t>(oe - 1 - crow0) : jr;
-            const int32_t st = static_cast<int32_t>((ob > j ? ob : j) - crow0);
-            const Acc<T> P = running_at(kl, st);
-            const int64_t len = oe > ob ? oe - ob : 0;
-            bool last = false;
-            int pc = 0;
-            if (valid) {
-                if (head_pending && s == Iu) {
-                    // began in an earlier unit: leave the head partial, join the ticket
-                    const C R = rows_here ? CO::then(carry, P) : carry;
-                    if constexpr (OP == OP_SUM && kIsFloat<T>) heads[u_me] = to_part(R);
-                    else heads[u_me] = to_part<T, OP>(R, Ru);
-                    __threadfence();
-                    const int64_t f = ob - o0 + Iu;
-                    pc = static_cast<int>(f / Wu);
-                    pc = pc < 0 ? 0 : (pc > u_me ? static_cast<int>(u_me) : pc);
-                    last = ticket_arrive(p.ws_tickets, static_cast<int>(u_me),
-                                         static_cast<int>(u_me) - pc + 1, p.gen);
-                    if (last) __threadfence();
-                } else {
-                    T v;
-                    int64_t a;
-                    if (len == 0) {
-                        v = T(0);
-                        a = -1;
-                    } else if (ob >= j) {
-                        finish_acc<T, OP>(P, len, mean, Ru, v, a);   // began in this tile
-                    } else {
-                        const C R = rows_here ? CO::then(carry, P) : carry;
-                        if constexpr (OP == OP_SUM && kIsFloat<T>) {
-                            finish_carry(R, len, mean, v);
-                            a = -1;
-                        } else {
-                            finish_acc<T, OP>(R, len, mean, Ru, v, a);
-                        }
-                    }
-                    out[s] = v;
-                    if (want_arg) p.out_arg[s] = a;
-                }
-            }
-            if (head_pending && k == 0) {
-                // the unit's first end sat on lane 0
-                last = __shfl_sync(0xffffffffu, last, 0);
-                pc = __shfl_sync(0xffffffffu, pc, 0);
-                const int64_t hl = __shfl_sync(0xffffffffu, len, 0);
-                if (last)
-                    warp_combine_store<T, OP>(p, tails, heads, pc, static_cast<int>(u_me), Iu, hl, lane);
-            }
-        }
-        if (n_e > 0) head_pending = false;
-        // the segment left open, es + n_e, starts at offsets[es + n_e]
-        {
-            const int l = (n_e - 1) & 31;
-            const int64_t e0 = __shfl_sync(0xffffffffu, E[0], l);
-            const int64_t e1 = __shfl_sync(0xffffffffu, E[1], l);
-            const int64_t bo = n_e == 0 ? b_es : (n_e <= 32 ? e0 : e1);
-            const int64_t sto = bo > j ? bo : j;
-            const bool rows_open = has_rows && sto < tr1;
-            const Acc<T> P = running_at(tr - 1, static_cast<int32_t>(sto - crow0));
-            if (rows_open)
-                carry = bo < j ? CO::then(carry, P) : CO::from(P);
-            else if (!(bo < j))
-                carry = CO::ident();
-            b_es = bo;
-        }
-        j = tr1;
-        es += n_e;
-        __syncwarp();
-        // hand back offsets chunks that hold only entries before es
-        if (lane == 0) {
-            while (odone < ow && os.A0 + static_cast<uint64_t>(odone + 1) * SW_OCHUNK <=
-                                     obase + static_cast<uint64_t>(es) * OSZ) {
-                if (o_issued < os.nch) {
-                    issue_chunk(os, o_issued, oring, SW_ORING, SW_OCHUNK, &fo[o_issued % SW_NSO], policy);
-                    ++o_issued;
-                }
-                ++odone;
-            }
-        }
-        odone = __shfl_sync(0xffffffffu, odone, 0);
-        o_issued = __shfl_sync(0xffffffffu, o_issued, 0);
     }
-    v_issued = __shfl_sync(0xffffffffu, v_issued, 0);
 
     // ---- a6: the segment still open at the end of the unit -------------------------
     if (ok && Iu2 < S) {
@@ -575,12 +679,12 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
             bool last = false;
             int pc = 0, qc = 0;
             if (lane == 0) {
-                if constexpr (OP == OP_SUM && kIsFloat<T>) tails[u_me] = to_part(carry);
+                if constexpr (kFloatSum) tails[u_me] = to_part(carry);
                 else tails[u_me] = to_part<T, OP>(carry, Ru);
                 __threadfence();
                 const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
-                const int64_t f = ob - o0 + Iu2;
-                const int64_t e = (oe > ob ? oe : ob) - o0 + Iu2;
+                const int64_t f = ob - o0 + SW_CW * Iu2;
+                const int64_t e = (oe > ob ? oe : ob) - o0 + SW_CW * Iu2;
                 pc = static_cast<int>(f / Wu);
                 qc = static_cast<int>(e / Wu);
                 pc = pc < 0 ? 0 : (pc > u_me ? static_cast<int>(u_me) : pc);
@@ -588,9 +692,9 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
                 last = qc < U && ticket_arrive(p.ws_tickets, qc, qc - pc + 1, p.gen);
                 if (last) __threadfence();
             }
-            last = __shfl_sync(0xffffffffu, last, 0);
-            pc = __shfl_sync(0xffffffffu, pc, 0);
-            qc = __shfl_sync(0xffffffffu, qc, 0);
+            last = __shfl_sync(FULL, last, 0);
+            pc = __shfl_sync(FULL, pc, 0);
+            qc = __shfl_sync(FULL, qc, 0);
             if (last) {
                 const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
                 warp_combine_store<T, OP>(p, tails, heads, pc, qc, Iu2, oe > ob ? oe - ob : 0, lane);
