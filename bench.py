@@ -35,7 +35,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "segmented-reduce effective HBM GB/s and % of GB300 peak; segments/s (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["ptx.cuh", "seg_common.cuh", "seg_rows.cuh", "seg_scalar.cuh", "seg_pick.cuh", "api.cu"]
+KERNEL_SOURCES = ["ptx.cuh", "seg_common.cuh", "seg_rows2.cuh", "seg_scalar.cuh", "seg_pick.cuh", "api.cu"]
 
 
 def kernel_hash() -> str:

@@ -120,16 +120,16 @@ seg_status_t seg_reduce_device_status(seg_stream_t stream);
  * its alignment matters) and `sm_count` the device's multiprocessor count.
  */
 typedef struct {
-    int32_t grid;            /* CTAs launched (at most one per SM)                    */
-    int32_t block;           /* threads per CTA: consumer warps + one producer warp   */
-    int32_t slot_threads;    /* threads that share one row (G)                        */
-    int32_t items_per_slot;  /* merge items (rows + segment ends) per slot per tile   */
-    int32_t vec;             /* elements per shared-memory load (1 or 4)              */
-    int32_t vecs_per_thread; /* load groups per thread per row                        */
-    int32_t max_ends;        /* cap on segment ends in one tile                       */
-    int32_t kernel_variant;  /* index of the compiled kernel shape                    */
-    int64_t smem_bytes;      /* dynamic shared memory per CTA                         */
-    int64_t workspace_bytes; /* library-owned scratch the launch uses                 */
+    int32_t grid;            /* CTAs launched (at most one per SM)                         */
+    int32_t block;           /* threads per CTA (one work unit per warp)                   */
+    int32_t slot_threads;    /* lanes that work on one row (scalar kernel: 1)              */
+    int32_t items_per_slot;  /* scalar: rows per lane per tile; rows: rows in flight       */
+    int32_t vec;             /* 32-bit elements per load                                   */
+    int32_t vecs_per_thread; /* column slices a row is cut into (scalar kernel: 1)         */
+    int32_t max_ends;        /* scalar: segment ends per tile at most; rows: 0             */
+    int32_t kernel_variant;  /* index of the compiled kernel shape                         */
+    int64_t smem_bytes;      /* dynamic shared memory per CTA                              */
+    int64_t workspace_bytes; /* library-owned scratch the launch uses                      */
 } seg_plan_t;
 
 seg_status_t seg_reduce_plan(seg_dtype_t dtype, int64_t F, int64_t num_values,
@@ -162,13 +162,16 @@ seg_status_t seg_reduce_plan(seg_dtype_t dtype, int64_t F, int64_t num_values,
  *                 library that nothing reads.  seg_reduce_device_status does
  *                 not see errors of this call.
  *
- * Limit.  The scratch a launch needs grows with the grid and, for row
- * tensors, with F: (ticket words: SM count * 128 bytes rounded up to 256) +
- * (partials: 2 * grid * 16 * 16 bytes for F == 1, 2 * grid * F * 16 bytes
- * for F > 1).  On a 152-SM GPU every F == 1 call fits, and F > 1 fits up to
- * F = 858 at a full grid (seg_reduce_plan reports workspace_bytes).  A call
- * that would need more returns SEG_ERR_SCRATCH_LIMIT before launching
- * anything; use seg_reduce for it.
+ * Limit.  The scratch a launch needs grows with the grid: (ticket words:
+ * SM count * 128 bytes rounded up to 256) + (partials: 2 * grid * 16 * 16
+ * bytes for F == 1; 2 * grid * 8 * 32 * vec * (4, or 12 for min / max)
+ * bytes for F > 1, grid and vec being seg_reduce_plan's).  On a 152-SM GPU
+ * every F == 1 call, every sum and mean, and min / max on rows loaded at
+ * most two columns at a time fit; min / max on rows loaded four columns at
+ * a time (F >= 128, F % 4 == 0, 16-byte aligned rows) fit while the grid is
+ * at most 84 CTAs (seg_reduce_plan reports workspace_bytes).  A call that
+ * would need more returns SEG_ERR_SCRATCH_LIMIT before launching anything;
+ * use seg_reduce for it.
  *
  * Set-up.  The first call on each device looks up the array's address
  * (cudaGetSymbolAddress, with that device current), clears its ticket words
@@ -188,7 +191,7 @@ seg_status_t seg_reduce_plan(seg_dtype_t dtype, int64_t F, int64_t num_values,
  * between them, or different host threads) race on it and give wrong
  * results; order them on one stream, or synchronise between them.
  */
-#define SEG_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define SEG_NOALLOC_SCRATCH_BYTES (2u << 20)
 
 seg_status_t seg_reduce_noalloc(const void *values, seg_dtype_t dtype, int64_t F,
                                 int64_t num_values, const void *offsets,

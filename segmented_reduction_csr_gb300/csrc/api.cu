@@ -31,12 +31,6 @@ int64_t ticket_region_bytes(int32_t sm_count) {
     return ceil_div(int64_t(sm_count) * SW_NW * 8, 256) * 256;
 }
 
-int32_t next_pow2(int32_t x) {
-    int32_t p = 1;
-    while (p < x) p <<= 1;
-    return p;
-}
-
 // ---------------------------------------------------------------------------
 // Planner (host only).
 
@@ -53,7 +47,6 @@ seg_status_t plan_launch(seg_dtype_t dtype, int64_t F, int64_t num_values,
     if (offsets_dtype == SEG_OFF_U32 && num_values > int64_t(UINT32_MAX)) return SEG_ERR_INVALID_ARGUMENT;
 
     std::memset(pl, 0, sizeof(*pl));
-    const int64_t items = num_values + S;
     if (F == 1) {
         // the scalar kernel: SW_NW warp units per CTA, each at least two chunks of
         // rows; a segment end weighs SW_CW rows in the partition
@@ -74,39 +67,43 @@ seg_status_t plan_launch(seg_dtype_t dtype, int64_t F, int64_t num_values,
         pl->workspace_bytes = ticket_region_bytes(sm_count) + 2 * grid * SW_NW * int64_t(sizeof(PartElem));
         return SEG_OK;
     }
-    const int64_t esz = F * 4;
-    int32_t shape, vec, nv, G;
-    if (F % 4 == 0 && values_addr % 16 == 0) {
-        const int32_t groups = static_cast<int32_t>(F / 4);
-        nv = groups <= NT ? 1 : 2;
-        shape = nv == 1 ? SHAPE_VEC4_NV1 : SHAPE_VEC4_NV2;
-        vec = 4;
-        G = std::min<int32_t>(NT, next_pow2(static_cast<int32_t>(ceil_div(groups, nv))));
-    } else {
-        nv = F <= NT ? 1 : 8;
-        shape = nv == 1 ? SHAPE_VEC1_NV1 : SHAPE_VEC1_NV8;
-        vec = 1;
-        G = std::min<int32_t>(NT, next_pow2(static_cast<int32_t>(ceil_div(F, nv))));
-    }
-    const int32_t nslots = NT / G;
-    const int64_t budget = int64_t(VRING) - 2 * int64_t(VCHUNK);
-    const int32_t K = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(32, budget / (nslots * esz))));
-    const int64_t T = int64_t(nslots) * K;
-    const int32_t max_ends = static_cast<int32_t>(std::min<int64_t>(1024, T));
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(sm_count, ceil_div(items, T)));
-    // Rows of one CTA are addressed with 32-bit offsets inside the CTA.
-    if (ceil_div(items, grid) + T >= int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;
+    // the row kernel: a warp per (column slice, merge range) unit.  VEC is the
+    // widest load that still gives all 32 lanes a column; narrow rows fall
+    // back to one column per lane so that more rows are in flight.
+    // Rows of a 16-byte multiple up to 128 columns are staged through shared
+    // memory by bulk copies (one slice; VEC just covers F).
+    const bool staged = F % 4 == 0 && values_addr % 16 == 0 && F <= 128;
+    int32_t vec = 1;
+    if (staged) vec = F > 64 ? 4 : (F > 32 ? 2 : 1);
+    else if (F % 4 == 0 && values_addr % 16 == 0 && F >= 128) vec = 4;
+    else if (F % 2 == 0 && values_addr % 8 == 0 && F >= 64) vec = 2;
+    const int64_t nsl = ceil_div(F, int64_t(32) * vec);           // column slices
+    const int64_t witems = num_values + int64_t(RW_CW) * S;
+    const int64_t ranges = std::max<int64_t>(1, ceil_div(witems, RW_MIN_ITEMS));
+    int64_t grid = ceil_div(ranges * nsl, RW_NW);
+    grid = std::max<int64_t>(grid, ceil_div(nsl, RW_NW));           // every slice gets a unit
+    grid = std::min<int64_t>(grid, std::max<int64_t>(sm_count, ceil_div(nsl, RW_NW)));
+    if (grid > sm_count) return SEG_ERR_UNSUPPORTED;               // tickets: one slot per unit
+    const int64_t units = grid * RW_NW;
+    const int64_t nr = units / nsl;                                 // ranges per slice
+    // a range's rows are addressed with 32-bit offsets inside the range
+    if (ceil_div(witems, nr) + 64 >= int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;
+    const int64_t slw = int64_t(32) * vec;
+    const int64_t part_bytes = 4 + ((op == SEG_MIN || op == SEG_MAX) ? 8 : 0);
 
     pl->grid = static_cast<int32_t>(grid);
-    pl->block = NTHREADS;
-    pl->slot_threads = G;
-    pl->items_per_slot = K;
+    pl->block = RW_NTHREADS;
+    pl->slot_threads = 32;
+    pl->items_per_slot = staged ? static_cast<int32_t>(RW_CB / (F * 4)) : (vec == 4 ? 16 : 32);
     pl->vec = vec;
-    pl->vecs_per_thread = nv;
-    pl->max_ends = max_ends;
-    pl->kernel_variant = shape;
-    pl->smem_bytes = SmemLayout::total(vec * nv);
-    pl->workspace_bytes = ticket_region_bytes(sm_count) + 2 * grid * F * int64_t(sizeof(PartElem));
+    pl->vecs_per_thread = static_cast<int32_t>(nsl);
+    pl->max_ends = 0;
+    if (staged)
+        pl->kernel_variant = vec == 4 ? SHAPE_STAGED_VEC4 : (vec == 2 ? SHAPE_STAGED_VEC2 : SHAPE_STAGED_VEC1);
+    else
+        pl->kernel_variant = vec == 4 ? SHAPE_ROWS_VEC4 : (vec == 2 ? SHAPE_ROWS_VEC2 : SHAPE_ROWS_VEC1);
+    pl->smem_bytes = staged ? RW_SMEM_STAGED : RW_SMEM;
+    pl->workspace_bytes = ticket_region_bytes(sm_count) + 2 * units * slw * part_bytes;
     return SEG_OK;
 }
 
@@ -183,7 +180,7 @@ seg_status_t scratch_for(int dev, cudaStream_t stream, size_t bytes, Scratch** o
 static __device__ __align__(256) unsigned char g_fixed_scratch[SEG_NOALLOC_SCRATCH_BYTES];
 static __device__ unsigned int g_fixed_status;   // device errors when the caller passes no word
 
-constexpr int kMaxKernels = 128;   // compiled kernels: 3 dtypes x 3 ops x 2 offset types x 5 shapes
+constexpr int kMaxKernels = 128;   // compiled kernels: 3 dtypes x 3 ops x 2 offset types x 7 shapes
 
 struct FixedState {
     bool init = false;
@@ -304,7 +301,7 @@ seg_status_t seg_reduce(const void* values, seg_dtype_t dtype, int64_t F, int64_
     prm.N = num_values;
     prm.S = S;
     prm.F = static_cast<int32_t>(F);
-    prm.G = pl.slot_threads;
+    prm.G = F > 1 ? pl.vecs_per_thread : 1;   // rows kernel: column slices
     prm.K = pl.items_per_slot;
     prm.max_ends = pl.max_ends;
     prm.P = pl.grid;
@@ -431,7 +428,7 @@ seg_status_t seg_reduce_noalloc(const void* values, seg_dtype_t dtype, int64_t F
     prm.N = num_values;
     prm.S = S;
     prm.F = static_cast<int32_t>(F);
-    prm.G = pl.slot_threads;
+    prm.G = F > 1 ? pl.vecs_per_thread : 1;   // rows kernel: column slices
     prm.K = pl.items_per_slot;
     prm.max_ends = pl.max_ends;
     prm.P = pl.grid;

@@ -3,29 +3,33 @@
 // own translation unit (seg_u32.cu, seg_s32.cu, seg_f32.cu) so the builds
 // run in parallel.
 #pragma once
-#include "seg_rows.cuh"
+#include "seg_rows2.cuh"
 #include "seg_scalar.cuh"
 
 namespace segred {
 
-// Kernel shapes; the host planner picks one (seg_reduce_plan_t::kernel_variant).
+// Kernel shapes; the host planner picks one (seg_plan_t::kernel_variant).
 enum : int {
-    SHAPE_VEC1_NV1 = 0,  // F == 1, or F <= 256 without 16-byte rows
-    SHAPE_VEC1_NV8 = 1,  // F <= 2048 without 16-byte rows
-    SHAPE_VEC4_NV1 = 2,  // F % 4 == 0, F <= 1024, 16-byte aligned values
-    SHAPE_VEC4_NV2 = 3,  // F % 4 == 0, F <= 2048, 16-byte aligned values
-    SHAPE_SCALAR = 4,    // F == 1: the scalar kernel
-    SHAPE_COUNT = 5
+    SHAPE_ROWS_VEC1 = 0,    // F > 1: one 32-bit column per lane, register ring
+    SHAPE_ROWS_VEC2 = 1,    // F > 1, F even, 8-byte aligned rows: two columns per lane
+    SHAPE_ROWS_VEC4 = 2,    // F > 1, F % 4 == 0, 16-byte aligned rows: four columns per lane
+    SHAPE_SCALAR = 4,       // F == 1: the scalar kernel
+    SHAPE_STAGED_VEC1 = 5,  // 1 < F <= 32, F % 4 == 0, 16-byte aligned: rows staged by bulk copies
+    SHAPE_STAGED_VEC2 = 6,  // 32 < F <= 64, same
+    SHAPE_STAGED_VEC4 = 7,  // 64 < F <= 128, same
+    SHAPE_COUNT = 8
 };
 
 template <class T, int OP, class OffT>
 const void* pick_shape(int shape) {
     switch (shape) {
-        case SHAPE_VEC1_NV1: return reinterpret_cast<const void*>(&seg_rows_kernel<T, OP, OffT, 1, 1>);
-        case SHAPE_VEC1_NV8: return reinterpret_cast<const void*>(&seg_rows_kernel<T, OP, OffT, 1, 8>);
-        case SHAPE_VEC4_NV1: return reinterpret_cast<const void*>(&seg_rows_kernel<T, OP, OffT, 4, 1>);
-        case SHAPE_VEC4_NV2: return reinterpret_cast<const void*>(&seg_rows_kernel<T, OP, OffT, 4, 2>);
+        case SHAPE_ROWS_VEC1: return reinterpret_cast<const void*>(&seg_rows2_kernel<T, OP, OffT, 1, false>);
+        case SHAPE_ROWS_VEC2: return reinterpret_cast<const void*>(&seg_rows2_kernel<T, OP, OffT, 2, false>);
+        case SHAPE_ROWS_VEC4: return reinterpret_cast<const void*>(&seg_rows2_kernel<T, OP, OffT, 4, false>);
         case SHAPE_SCALAR: return reinterpret_cast<const void*>(&seg_scalar_kernel<T, OP, OffT>);
+        case SHAPE_STAGED_VEC1: return reinterpret_cast<const void*>(&seg_rows2_kernel<T, OP, OffT, 1, true>);
+        case SHAPE_STAGED_VEC2: return reinterpret_cast<const void*>(&seg_rows2_kernel<T, OP, OffT, 2, true>);
+        case SHAPE_STAGED_VEC4: return reinterpret_cast<const void*>(&seg_rows2_kernel<T, OP, OffT, 4, true>);
         default: return nullptr;
     }
 }

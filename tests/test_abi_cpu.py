@@ -82,24 +82,29 @@ def test_plan_shapes(lib):
     assert p["smem_bytes"] <= 227 * 1024
     assert p["workspace_bytes"] >= 152 * 16 * 8 + 2 * 152 * 16 * 16  # unit tickets + partials
     p = sr.plan("f32", 64, 1_000_000, "i64", 10_000, "max", values_addr=256, sm_count=152)
-    assert p["vec"] == 4 and p["slot_threads"] == 16 and p["vecs_per_thread"] == 1
+    assert p["vec"] == 2 and p["slot_threads"] == 32 and p["vecs_per_thread"] == 1
+    assert p["grid"] == 152 and p["block"] == 256
+    p = sr.plan("f32", 128, 1_000_000, "i64", 10_000, "sum", values_addr=256, sm_count=152)
+    assert p["vec"] == 4 and p["vecs_per_thread"] == 1
     p = sr.plan("f32", 64, 1_000_000, "i64", 10_000, "max", values_addr=260, sm_count=152)
-    assert p["vec"] == 1                                 # misaligned rows: scalar path
+    assert p["vec"] == 1 and p["vecs_per_thread"] == 2        # misaligned rows: one column per lane
     p = sr.plan("f32", 2048, 1000, "i64", 10, "sum", values_addr=256, sm_count=152)
-    assert p["vecs_per_thread"] == 2 and p["slot_threads"] == 256
+    assert p["vec"] == 4 and p["vecs_per_thread"] == 16
     p = sr.plan("f32", 130, 1000, "i64", 10, "sum", values_addr=256, sm_count=152)
-    assert p["vec"] == 1 and p["slot_threads"] == 256
+    assert p["vec"] == 2 and p["vecs_per_thread"] == 3
     p = sr.plan("u32", 1, 100, "u32", 10, "min", sm_count=152)
     assert p["grid"] == 1                                # tiny input: one CTA
-    for F in (1, 2, 3, 5, 8, 64, 100, 128, 130, 1000, 1024, 2048):
+    for F in (2, 3, 5, 8, 64, 100, 128, 130, 1000, 1024, 2048):
         for addr in (256, 260):
-            p = sr.plan("f32", F, 10_000_000, "i64", 100_000, "max", values_addr=addr)
-            T = (256 // p["slot_threads"]) * p["items_per_slot"]
-            # a tile's rows plus two partial chunks fit the 128 KiB value ring
-            assert T * F * 4 + 2 * 8192 <= 128 * 1024 or F == 1
-            assert p["smem_bytes"] <= 227 * 1024
-            assert p["slot_threads"] * p["vec"] * p["vecs_per_thread"] >= F
-            assert p["workspace_bytes"] >= 2 * p["grid"] * F * 16
+            for op in ("sum", "max"):
+                p = sr.plan("f32", F, 10_000_000, "i64", 100_000, op, values_addr=addr)
+                assert p["smem_bytes"] <= 227 * 1024
+                assert 32 * p["vec"] * p["vecs_per_thread"] >= F > 32 * p["vec"] * (p["vecs_per_thread"] - 1)
+                assert addr % (4 * p["vec"]) == 0 and F % p["vec"] == 0
+                units = p["grid"] * p["block"] // 32
+                assert units >= p["vecs_per_thread"]
+                per = 4 + (8 if op == "max" else 0)
+                assert p["workspace_bytes"] >= 2 * units * 32 * p["vec"] * per
 
 
 def test_plan_rejects(lib):

@@ -101,20 +101,20 @@ def test_noalloc_allocates_nothing():
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
-    """Wide rows at a full grid need more than the fixed array: a clear error,
-    nothing launched (the output keeps its sentinel)."""
+    """Wide rows with min / max on a large grid need more than the fixed
+    array: a clear error, nothing launched (the output keeps its sentinel)."""
     import torch
     import segmented_reduction_csr_gb300 as sr
     feat = 2048
-    n, s = 40_000, 100
+    n, s = 50_000, 100
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    need = sr.plan("f32", feat, n, "i64", s, "sum", values_addr=256, sm_count=sms)["workspace_bytes"]
+    need = sr.plan("f32", feat, n, "i64", s, "max", values_addr=256, sm_count=sms)["workspace_bytes"]
     assert need > sr.NOALLOC_SCRATCH_BYTES
     dv = torch.zeros((n, feat), dtype=torch.float32, device="cuda")
     do = torch.linspace(0, n, s + 1, device="cuda").to(torch.int64)
     out = torch.full((s, feat), 3.0, device="cuda")
     with pytest.raises(sr.SegReduceError) as ei:
-        sr.seg_reduce_noalloc(dv, do, "sum", out)
+        sr.seg_reduce_noalloc(dv, do, "max", out)
     assert ei.value.status == 6
     torch.cuda.synchronize()
     assert bool((out == 3.0).all())
