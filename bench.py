@@ -344,7 +344,8 @@ def run_ours(args, w: W.Workload):
         "segments_per_s": world * w.num_segments * len(cases) * args.steps / (kernel_ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "segred::seg_reduce_kernel (all instantiations of the step)",
+                     "kernel": ("segred::seg_scalar_kernel" if w.feat == 1 else "segred::seg_rows2_kernel")
+                               + " (every launch of the step)",
                      "peak_note": f"{peak_kind} HBM copy bandwidth"},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

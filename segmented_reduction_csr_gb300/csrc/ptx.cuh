@@ -1,6 +1,6 @@
 // ptx.cuh -- thin inline-PTX wrappers used by the segmented-reduction
 // kernels: mbarrier phases, the 1-D bulk async copy (global -> shared,
-// completion counted on an mbarrier), named barriers for the consumer warps,
+// completion counted on an mbarrier), the L2 bulk prefetch, proxy fences
 // and the global nanosecond timer for bounded waits.  sm_90+ (built for
 // sm_103a).
 #pragma once
@@ -28,11 +28,6 @@ __device__ __forceinline__ void fence_mbarrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
 // One arrival plus `bytes` of expected transaction count.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
@@ -47,19 +42,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Non-blocking test of the same condition.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -94,27 +76,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
-}
-
-// Named barrier 1 over the first `n` threads (the consumer warps).
-template <int n>
-__device__ __forceinline__ void named_bar_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(n) : "memory");
-}
-
-// Named barrier 1 over `n` threads that also ANDs a predicate across them.
-template <int n>
-__device__ __forceinline__ bool named_bar_and(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred a, b;\n\t"
-        "setp.ne.u32 a, %1, 0;\n\t"
-        "bar.red.and.pred b, 1, %2, a;\n\t"
-        "selp.u32 %0, 1, 0, b;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "n"(n)
-        : "memory");
-    return r != 0;
 }
 
 __device__ __forceinline__ uint32_t ld_global_u32(uint64_t addr) {

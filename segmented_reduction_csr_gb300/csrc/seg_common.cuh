@@ -8,17 +8,12 @@
 // [N, F] rows reduce per column, min / max also return the source row (ties to
 // the lower row, -1 when empty), mean = sum / length.
 //
-// The work unit.  The items are the rows of [offsets[0], offsets[S]) and
-// the S segment ends, merged in order: row r of segment s sits at merge
-// position (r - o0) + s and the end of segment s at (offsets[s+1] - o0) + s.
-// The merge-based partition that graph-reduce's README cites (Merrill and
-// Garland 2016) gives every CTA the same number of items whatever the segment
-// lengths -- the fix for the long, skewed segments that the luma page warns
-// serialise on one workgroup.  One persistent CTA per SM owns a contiguous
-// range of merge positions; a producer warp streams its rows and offsets
-// through shared-memory rings with 1-D bulk copies; a segment that crosses
-// CTAs leaves per-CTA partials in scratch and the last CTA to arrive (an
-// atomic ticket, never a wait) combines them in CTA order.
+// The kernels (seg_scalar.cuh, seg_rows2.cuh) cut the merged sequence of
+// rows and segment ends into equal-weight units, one per warp, and combine
+// the segments that cross units through per-unit partials and an atomic
+// ticket (never a wait).  This file holds what they share: the launch
+// parameters, element arithmetic, the partial format, the bulk-copy stream
+// geometry, bounded waits and the ticket.
 #pragma once
 #include <climits>
 #include <cstdint>
@@ -30,11 +25,9 @@ namespace segred {
 
 enum : int { OP_SUM = 0, OP_MIN = 1, OP_MAX = 2 };
 
-constexpr int SEARCH_PPT = 4;        // probes per thread per search round
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 constexpr unsigned STATUS_CONSUMER_TIMEOUT = 1u;
-constexpr unsigned STATUS_PRODUCER_TIMEOUT = 2u;
 constexpr unsigned STATUS_DRAIN_TIMEOUT = 4u;
 
 struct Params {
@@ -45,13 +38,13 @@ struct Params {
     int64_t N;        // rows in values
     int64_t S;        // segments
     int32_t F;        // columns
-    int32_t G;        // threads per slot (power of two, <= NT)
-    int32_t K;        // merge items per slot per tile
-    int32_t max_ends; // cap on segment ends per tile (offsets window)
+    int32_t G;        // row kernel: column slices
+    int32_t K;        // rows per lane per tile / rows in flight (informational)
+    int32_t max_ends; // segment ends per tile (informational)
     int32_t P;        // CTAs in the grid
     int32_t mean;     // finalise sums as means
-    void* ws_parts;   // [2][P][F] PartElem: CTA tail partials, then CTA head partials
-    unsigned long long* ws_tickets;  // [P], (generation << 32) | arrivals
+    void* ws_parts;   // unit tail partials, then unit head partials
+    unsigned long long* ws_tickets;  // one per unit: (generation << 32) | arrivals
     unsigned int* status;            // device status word
     uint32_t gen;                    // call generation, > 0, increasing per scratch buffer
 };
@@ -122,8 +115,7 @@ struct Red {
     }
 };
 
-// Running value of the segment that is still open at a tile boundary.  Float
-// sums carry in double, so long chains of tile partials add no float32 error.
+// Running value of the segment that is still open at a tile boundary.
 template <class T, int OP>
 struct Carry {
     using C = Acc<T>;
@@ -133,21 +125,6 @@ struct Carry {
         return Red<T, OP>::comb(c, a);
     }
 };
-struct CarryD {
-    double v;
-};
-template <>
-struct Carry<float, OP_SUM> {
-    using C = CarryD;
-    __device__ __forceinline__ static C ident() { return C{0.0}; }
-    __device__ __forceinline__ static C from(const Acc<float>& a) {
-        return C{static_cast<double>(a.v)};
-    }
-    __device__ __forceinline__ static C then(const C& c, const Acc<float>& a) {
-        return C{c.v + static_cast<double>(a.v)};
-    }
-};
-
 // The scalar kernel's float-sum carry: a compensated pair (hi + lo) kept
 // with TwoSum (Knuth), so a long chain of tile partials stays within a few
 // units of 2^-48 of the exact sum while using only float32 arithmetic.
@@ -196,12 +173,6 @@ __device__ __forceinline__ void finish_acc(const Acc<T>& a, int64_t len, int mea
         arg = a.row >= 0 ? row_base + a.row : -1;
     }
 }
-__device__ __forceinline__ void finish_carry(const CarryD& c, int64_t len, int mean, float& v) {
-    const float s = static_cast<float>(c.v);
-    v = mean ? (len > 0 ? s / static_cast<float>(len) : 0.0f) : s;
-}
-
-// Partials in scratch.
 template <class T, int OP>
 __device__ __forceinline__ PartElem to_part(const Acc<T>& a, int64_t row_base) {
     PartElem p;
@@ -216,12 +187,6 @@ __device__ __forceinline__ void finish_carry(const CarryF2& c, int64_t len, int 
 __device__ __forceinline__ PartElem to_part(const CarryF2& c) {
     PartElem p;
     p.v.d = static_cast<double>(c.hi) + static_cast<double>(c.lo);
-    p.row = -1;
-    return p;
-}
-__device__ __forceinline__ PartElem to_part(const CarryD& c) {
-    PartElem p;
-    p.v.d = c.v;
     p.row = -1;
     return p;
 }
@@ -247,10 +212,8 @@ __device__ __forceinline__ void finish_part(const PartElem& p, int64_t len, int 
                                             int64_t& arg) {
     if constexpr (OP == OP_SUM) {
         if constexpr (kIsFloat<T>) {
-            CarryD c{p.v.d};
-            float f;
-            finish_carry(c, len, mean, f);
-            v = f;
+            const float f = static_cast<float>(p.v.d);
+            v = mean ? (len > 0 ? f / static_cast<float>(len) : 0.0f) : f;
         } else {
             v = from_bits<T>(p.v.u);
         }
@@ -332,63 +295,6 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uns
     }
 }
 
-// The producer thread: streams chunk after chunk of both byte ranges into
-// their rings, never blocking on one ring while the other has a free stage.
-template <uint32_t VR, uint32_t VC, uint32_t OR, uint32_t OC>
-__device__ __forceinline__ void producer_loop(const Stream& vs, const Stream& os,
-                                              unsigned char* vring, unsigned char* oring,
-                                              uint64_t* full_v, uint64_t* empty_v,
-                                              uint64_t* full_o, uint64_t* empty_o,
-                                              unsigned int* status) {
-    constexpr int NSV = VR / VC;
-    constexpr int NSO = OR / OC;
-    const uint64_t policy = policy_evict_first();
-    int64_t mv = 0, mo = 0;
-    uint64_t t_last = 0;
-    int idle = 0;
-    while (mv < vs.nch || mo < os.nch) {
-        bool progressed = false;
-        if (mo < os.nch &&
-            (mo < NSO || mbar_test_wait(&empty_o[mo % NSO], static_cast<uint32_t>((mo / NSO - 1) & 1)))) {
-            issue_chunk(os, mo, oring, OR, OC, &full_o[mo % NSO], policy);
-            ++mo;
-            progressed = true;
-        }
-        if (mv < vs.nch &&
-            (mv < NSV || mbar_test_wait(&empty_v[mv % NSV], static_cast<uint32_t>((mv / NSV - 1) & 1)))) {
-            issue_chunk(vs, mv, vring, VR, VC, &full_v[mv % NSV], policy);
-            ++mv;
-            progressed = true;
-        }
-        if (progressed) {
-            idle = 0;
-            t_last = 0;   // the time limit counts from the last progress
-            continue;
-        }
-        if (++idle >= 32) {
-            idle = 0;
-            const uint64_t now = globaltimer_ns();
-            if (t_last == 0) t_last = now;
-            if (now - t_last > WAIT_LIMIT_NS) {
-                atomicOr(status, STATUS_PRODUCER_TIMEOUT);
-                break;
-            }
-            __nanosleep(32);
-        }
-    }
-    // Every copy this thread started must land before the CTA may exit.
-    for (int64_t m = (mv > NSV ? mv - NSV : 0); m < mv; ++m)
-        wait_bounded(&full_v[m % NSV], static_cast<uint32_t>((m / NSV) & 1), status, STATUS_DRAIN_TIMEOUT);
-    for (int64_t m = (mo > NSO ? mo - NSO : 0); m < mo; ++m)
-        wait_bounded(&full_o[m % NSO], static_cast<uint32_t>((m / NSO) & 1), status, STATUS_DRAIN_TIMEOUT);
-}
-
-// Initialises the per-stage full / empty mbarriers of both rings (one thread).
-__device__ __forceinline__ void init_ring_barriers(uint64_t* bars, int nsv, int nso) {
-    for (int k = 0; k < 2 * (nsv + nso); ++k) mbar_init(&bars[k], 1);
-    fence_mbarrier_init();
-}
-
 template <class OffT>
 __device__ __forceinline__ int64_t clamp_off(OffT raw, int64_t N) {
     int64_t o = static_cast<int64_t>(raw);
@@ -396,7 +302,7 @@ __device__ __forceinline__ int64_t clamp_off(OffT raw, int64_t N) {
     return o > N ? N : o;
 }
 
-// Cross-CTA arrival for the segment whose end lies in CTA q; true for the
+// Cross-unit arrival for the segment whose end lies in unit q; true for the
 // last of `expected` contributors.  Tickets carry the call generation in the
 // high half, so a stale count left by an earlier call is reset, not used.
 __device__ __forceinline__ bool ticket_arrive(unsigned long long* tickets, int q, int expected,
@@ -413,124 +319,6 @@ __device__ __forceinline__ PartElem load_part(const PartElem* src) {
     pe.v.d = raw.x;
     pe.row = __double_as_longlong(raw.y);
     return pe;
-}
-
-// Last arriver for segment s: tails of CTAs pc .. qc-1, then the head of CTA
-// qc, combined in CTA order (so float sums are reproducible), then stored.
-template <class T, int OP>
-__device__ __forceinline__ void combine_store(const Params& p, const PartElem* tails,
-                                              const PartElem* heads, int pc, int qc, int64_t s,
-                                              int64_t len, int tid, int nthreads) {
-    const int F = p.F;
-    T* out = static_cast<T*>(p.out);
-    for (int col = tid; col < F; col += nthreads) {
-        PartElem a = load_part(pc < qc ? &tails[static_cast<int64_t>(pc) * F + col]
-                                       : &heads[static_cast<int64_t>(qc) * F + col]);
-        for (int k = pc + 1; k <= qc; ++k)
-            a = part_comb<T, OP>(a, load_part(k < qc ? &tails[static_cast<int64_t>(k) * F + col]
-                                                     : &heads[static_cast<int64_t>(qc) * F + col]));
-        T v;
-        int64_t ar;
-        finish_part<T, OP>(a, len, p.mean, v, ar);
-        out[s * F + col] = v;
-        if (OP != OP_SUM && p.out_arg != nullptr) p.out_arg[s * F + col] = ar;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// a2: this CTA's share of the merge path.
-
-struct CtaRange {
-    int64_t o0, oS;     // clamped first / last offset
-    int64_t W;          // merge items per CTA
-    int64_t Dlo, Dhi;   // merge positions [Dlo, Dhi)
-    int64_t Ilo, Ihi;   // segment ends before Dlo / Dhi
-    int64_t Rlo, Rhi;   // rows before Dlo / Dhi (absolute)
-};
-
-// All NTH threads of the CTA call this with the same arguments.  I(D), the
-// number of segment ends before merge position D, is #{s : key(s) < D} with
-// key(s) = (offsets[s+1] - o0) + s increasing; each round probes
-// NTH * SEARCH_PPT evenly spaced keys for both Dlo and Dhi and keeps the
-// bracket, so S up to ~1.3M resolves in two rounds.  Returns false (for
-// every thread) when the CTA has no items.  `counts` is 6 ints of shared
-// memory, zeroed by the caller before a __syncthreads.
-template <int NTH, class OffT>
-__device__ __forceinline__ bool cta_range(const Params& p, int* counts, CtaRange& r) {
-    const int tid = threadIdx.x;
-    const int64_t N = p.N, S = p.S;
-    const OffT* offs = static_cast<const OffT*>(p.offsets);
-    r.o0 = clamp_off(__ldg(&offs[0]), N);
-    r.oS = clamp_off(__ldg(&offs[S]), N);
-    r.oS = r.oS < r.o0 ? r.o0 : r.oS;
-    const int64_t nrows = r.oS - r.o0;
-    const int64_t total = nrows + S;
-    r.W = (total + p.P - 1) / p.P;
-    const int64_t c = static_cast<int64_t>(blockIdx.x);
-    r.Dlo = c * r.W < total ? c * r.W : total;
-    r.Dhi = r.Dlo + r.W < total ? r.Dlo + r.W : total;
-    if (r.Dlo >= r.Dhi) return false;
-
-    int64_t lo[2], hi[2];
-    const int64_t Dq[2] = {r.Dlo, r.Dhi};
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        lo[q] = Dq[q] - nrows > 0 ? Dq[q] - nrows : 0;
-        hi[q] = Dq[q] < S ? Dq[q] : S;
-    }
-    constexpr int64_t NPTS = static_cast<int64_t>(NTH) * SEARCH_PPT;
-    for (int round = 0; round < 64; ++round) {
-        if (lo[0] >= hi[0] && lo[1] >= hi[1]) break;
-        int* cnt = counts + 2 * (round % 3);
-        int local[2];
-        int64_t step[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int64_t len = hi[q] - lo[q];
-            step[q] = (len + NPTS - 1) / NPTS;
-            local[q] = 0;
-            if (len > 0) {
-#pragma unroll
-                for (int u = 0; u < SEARCH_PPT; ++u) {
-                    const int64_t s = lo[q] + (static_cast<int64_t>(tid) * SEARCH_PPT + u) * step[q];
-                    if (s < hi[q]) {
-                        const int64_t key = clamp_off(__ldg(&offs[s + 1]), N) - r.o0 + s;
-                        local[q] += key < Dq[q] ? 1 : 0;
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int w = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(local[q]));
-            if ((tid & 31) == 0 && w) atomicAdd(&cnt[q], w);
-        }
-        if (tid == 0) {  // the buffer two rounds ahead was last read two barriers ago
-            counts[2 * ((round + 1) % 3) + 0] = 0;
-            counts[2 * ((round + 1) % 3) + 1] = 0;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            if (hi[q] - lo[q] <= 0) continue;
-            const int64_t cq = cnt[q];
-            if (cq == 0) {
-                hi[q] = lo[q];
-            } else {
-                const int64_t last = lo[q] + (cq - 1) * step[q];
-                const int64_t nh = last + step[q] < hi[q] ? last + step[q] : hi[q];
-                lo[q] = last + 1 < nh ? last + 1 : nh;
-                hi[q] = nh;
-            }
-        }
-    }
-    r.Ilo = lo[0];
-    r.Ihi = lo[1] > r.Ilo ? lo[1] : r.Ilo;
-    r.Rlo = r.Dlo - r.Ilo + r.o0;
-    r.Rlo = r.Rlo < r.o0 ? r.o0 : (r.Rlo > r.oS ? r.oS : r.Rlo);
-    r.Rhi = r.Dhi - r.Ihi + r.o0;
-    r.Rhi = r.Rhi < r.Rlo ? r.Rlo : (r.Rhi > r.oS ? r.oS : r.Rhi);
-    return true;
 }
 
 }  // namespace segred
