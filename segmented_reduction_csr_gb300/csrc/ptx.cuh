@@ -61,6 +61,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Per-thread asynchronous copy of 4 or 8 bytes from global to shared memory
+// (both aligned to the size); completion is awaited per thread with
+// cp_async_wait_all after cp_async_commit.
+template <int BYTES>
+__device__ __forceinline__ void cp_async_small(void* dst, const void* src) {
+    static_assert(BYTES == 4 || BYTES == 8, "4- or 8-byte copies");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)), "l"(src), "n"(BYTES)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Hint: bring `bytes` (multiple of 16) at global `src` (16-byte aligned) into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -71,6 +83,19 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
+
+// Ticket primitives: a relaxed max that returns nothing, an add with
+// release semantics (this thread's earlier writes are visible before the
+// add is) that returns the old value, and an acquire-release fence.
+__device__ __forceinline__ void red_max_relaxed_gpu(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long atom_add_release_gpu(unsigned long long* p, unsigned long long v) {
+    unsigned long long old;
+    asm volatile("atom.release.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;

@@ -302,15 +302,20 @@ __device__ __forceinline__ int64_t clamp_off(OffT raw, int64_t N) {
     return o > N ? N : o;
 }
 
-// Cross-unit arrival for the segment whose end lies in unit q; true for the
-// last of `expected` contributors.  Tickets carry the call generation in the
-// high half, so a stale count left by an earlier call is reset, not used.
-__device__ __forceinline__ bool ticket_arrive(unsigned long long* tickets, int q, int expected,
-                                              uint32_t gen) {
+// Cross-unit arrival for the segment whose end lies in unit q, in two halves
+// so that the caller can go on working while the atomic is in flight.
+// Tickets carry the call generation in the high half: a stale count left by
+// an earlier call is reset by the max, never used.  ticket_take returns the
+// old ticket value (the caller's own earlier writes are released with it);
+// ticket_last tells whether that arrival was the last of `expected`.  The
+// last arriver runs fence_acq_rel_gpu() before it reads the others' partials.
+__device__ __forceinline__ unsigned long long ticket_take(unsigned long long* tickets, int q, uint32_t gen) {
     const unsigned long long base = static_cast<unsigned long long>(gen) << 32;
-    atomicMax(&tickets[q], base);
-    const unsigned long long old = atomicAdd(&tickets[q], 1ull);
-    return old == base + static_cast<unsigned long long>(expected - 1);
+    red_max_relaxed_gpu(&tickets[q], base);
+    return atom_add_release_gpu(&tickets[q], 1ull);
+}
+__device__ __forceinline__ bool ticket_last(unsigned long long old, uint32_t gen, int expected) {
+    return old == (static_cast<unsigned long long>(gen) << 32) + static_cast<unsigned long long>(expected - 1);
 }
 
 __device__ __forceinline__ PartElem load_part(const PartElem* src) {

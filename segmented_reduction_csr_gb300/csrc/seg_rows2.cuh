@@ -372,25 +372,15 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
         }
         ecur = __shfl_sync(FULL, EB, k);
     };
-    // the head's ticket (its partial is out); the last arriver combines
+    // the head's ticket (its partial is out); the answer is read when the
+    // range is done, so the atomic's latency hides behind the rows
+    bool head_taken = false;
+    unsigned long long head_ticket = 0;   // lane 0
     auto head_flush = [&]() {
         __threadfence();
         __syncwarp();   // every lane's partial is out before the ticket
-        bool last = false;
-        int64_t pc = 0;
-        if (lane == 0) {
-            pc = (off_Iu - o0 + RW_CW * Iu) / Wr;
-            pc = pc < 0 ? 0 : (pc > rg ? rg : pc);
-            last = ticket_arrive(p.ws_tickets, static_cast<int>(u_me), static_cast<int>(rg - pc + 1), p.gen);
-            if (last) __threadfence();
-        }
-        last = __shfl_sync(FULL, last, 0);
-        pc = __shfl_sync(FULL, pc, 0);
-        if (last) {
-            const int64_t oe1 = clamp_off(__ldg(&offs[Iu + 1]), N);
-            rows_combine_store<T, OP, VEC>(p, pv, pr, U, NSL, slice, pc, rg, Iu,
-                                           oe1 > off_Iu ? oe1 - off_Iu : 0, lane);
-        }
+        if (lane == 0) head_ticket = ticket_take(p.ws_tickets, static_cast<int>(u_me), p.gen);
+        head_taken = true;
         head_saved = false;
     };
     // fold row r (relative), whose VEC elements are x
@@ -570,34 +560,51 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     if (head_saved) head_flush();
 
     // ---- the segment still open at the end of the range ---------------------------
+    // Its partial and ticket go out first; while that atomic is in flight the
+    // head ticket is read, and its segment combined if this range came last.
+    bool tail_taken = false;
+    unsigned long long tail_ticket = 0;
+    int64_t tpc = 0, tqc = 0, tob = 0;
     if (Iu2 < S) {
-        const int64_t ob = clamp_off(__ldg(&offs[Iu2]), N);
-        if (ob < Ru2) {
+        tob = clamp_off(__ldg(&offs[Iu2]), N);
+        if (tob < Ru2) {
             write_part(u_me);
             __threadfence();
             __syncwarp();   // every lane's partial is out before the ticket
-            bool last = false;
-            int64_t pc = 0, qc = 0;
             if (lane == 0) {
                 const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
-                const int64_t f = ob - o0 + RW_CW * Iu2;
-                const int64_t e = (oe > ob ? oe : ob) - o0 + RW_CW * Iu2;
-                pc = f / Wr;
-                qc = e / Wr;
-                pc = pc < 0 ? 0 : (pc > rg ? rg : pc);
-                qc = qc <= rg ? rg + 1 : qc;
-                last = qc < NR && ticket_arrive(p.ws_tickets, static_cast<int>(qc * NSL + slice),
-                                                static_cast<int>(qc - pc + 1), p.gen);
-                if (last) __threadfence();
+                const int64_t f = tob - o0 + RW_CW * Iu2;
+                const int64_t e = (oe > tob ? oe : tob) - o0 + RW_CW * Iu2;
+                tpc = f / Wr;
+                tqc = e / Wr;
+                tpc = tpc < 0 ? 0 : (tpc > rg ? rg : tpc);
+                tqc = tqc <= rg ? rg + 1 : tqc;
+                if (tqc < NR) tail_ticket = ticket_take(p.ws_tickets, static_cast<int>(tqc * NSL + slice), p.gen);
             }
-            last = __shfl_sync(FULL, last, 0);
-            pc = __shfl_sync(FULL, pc, 0);
-            qc = __shfl_sync(FULL, qc, 0);
-            if (last) {
-                const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
-                rows_combine_store<T, OP, VEC>(p, pv, pr, U, NSL, slice, pc, qc, Iu2, oe > ob ? oe - ob : 0,
-                                               lane);
-            }
+            tpc = __shfl_sync(FULL, tpc, 0);
+            tqc = __shfl_sync(FULL, tqc, 0);
+            tail_taken = tqc < NR;
+        }
+    }
+    if (head_taken) {
+        int64_t pc = (off_Iu - o0 + RW_CW * Iu) / Wr;
+        pc = pc < 0 ? 0 : (pc > rg ? rg : pc);
+        const bool last =
+            __shfl_sync(FULL, lane == 0 && ticket_last(head_ticket, p.gen, static_cast<int>(rg - pc + 1)), 0);
+        if (last) {
+            fence_acq_rel_gpu();
+            const int64_t oe1 = clamp_off(__ldg(&offs[Iu + 1]), N);
+            rows_combine_store<T, OP, VEC>(p, pv, pr, U, NSL, slice, pc, rg, Iu, oe1 > off_Iu ? oe1 - off_Iu : 0,
+                                           lane);
+        }
+    }
+    if (tail_taken) {
+        const bool last =
+            __shfl_sync(FULL, lane == 0 && ticket_last(tail_ticket, p.gen, static_cast<int>(tqc - tpc + 1)), 0);
+        if (last) {
+            fence_acq_rel_gpu();
+            const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
+            rows_combine_store<T, OP, VEC>(p, pv, pr, U, NSL, slice, tpc, tqc, Iu2, oe > tob ? oe - tob : 0, lane);
         }
     }
 }

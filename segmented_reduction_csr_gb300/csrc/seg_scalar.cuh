@@ -11,8 +11,10 @@
 //
 // Per warp.  Lane 0 streams the unit's rows (SW_VCHUNK-byte chunks, SW_NSV
 // stages, with the next chunks prefetched into L2 so that a refill finds them
-// there) and offsets (a SW_NSO-stage ring) into the warp's shared memory with
-// 1-D bulk copies, refilling a stage as soon as the warp is done with it.
+// there) into the warp's shared memory with 1-D bulk copies, refilling a
+// stage as soon as the warp is done with it.  The segment ends of the next
+// tile are copied by every lane (per-thread async copies, one entry each)
+// into the other half of a double buffer while the current tile runs.
 // A tile is the rows of one chunk plus the segment ends that fall in them (up
 // to SW_EMAXT ends; a chunk with more, which takes many empty segments, is
 // split into several tiles):
@@ -51,27 +53,23 @@ constexpr int SW_Q = SW_KR / 4;                // quads per lane
 constexpr int SW_TROWS = 32 * SW_KR;           // rows per value chunk
 constexpr uint32_t SW_VCHUNK = SW_TROWS * 4;   // bytes per value chunk
 constexpr int SW_NSV = 2;                      // value stages per warp
-constexpr uint32_t SW_OCHUNK = 512;            // bytes per offsets chunk
-constexpr int SW_NSO = 4;                      // offsets stages per warp
-constexpr uint32_t SW_ORING = SW_OCHUNK * SW_NSO;
 constexpr int SW_EMAXT = 160;                  // segment ends per tile
 constexpr int SW_NDIAG = SW_NW + 1;            // unit boundaries per CTA
 constexpr int SW_GRID = 1024;                  // first-round probes, shared by all CTAs
 constexpr int SW_PROBES = 60;                  // later-round probes per boundary
 static_assert(SW_Q % 2 == 1, "conflict-free 128-bit row loads need SW_KR / 4 odd");
 static_assert(SW_NDIAG * SW_PROBES <= 2 * SW_NTHREADS, "two probes per thread per round");
-static_assert((SW_EMAXT + 1) * 8 + SW_OCHUNK <= SW_ORING, "offsets ring holds a tile's window");
 static_assert(SW_EMAXT % 32 == 0, "ends are taken 32 at a time");
 
 // Per-warp shared memory.
 struct WarpSmem {
     static constexpr uint32_t vstage = 0;
-    static constexpr uint32_t oring = SW_NSV * SW_VCHUNK;
-    static constexpr uint32_t xs = oring + SW_ORING;        // [32] lane prefix values
+    static constexpr uint32_t obuf = SW_NSV * SW_VCHUNK;    // [2][SW_EMAXT] offsets (8 bytes each)
+    static constexpr uint32_t xs = obuf + 2 * SW_EMAXT * 8; // [32] lane prefix values
     static constexpr uint32_t xr = xs + 32 * 4;             // [32] lane prefix rows
     static constexpr uint32_t argr = xr + 32 * 4;           // [SW_TROWS] int16; start flags
     static constexpr uint32_t bars = argr + SW_TROWS * 2;
-    static constexpr uint32_t bytes = ((bars + (SW_NSV + SW_NSO) * 8 + 127) / 128) * 128;
+    static constexpr uint32_t bytes = ((bars + SW_NSV * 8 + 127) / 128) * 128;
 };
 constexpr uint32_t SW_SMEM = SW_NW * WarpSmem::bytes;
 static_assert(SW_SMEM <= 227 * 1024, "one CTA per SM");
@@ -253,7 +251,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     // ---- per-warp state ----------------------------------------------------------
     unsigned char* wbase = smem + warp * WarpSmem::bytes;
     unsigned char* vst = wbase + WarpSmem::vstage;
-    unsigned char* oring = wbase + WarpSmem::oring;
+    unsigned char* obuf = wbase + WarpSmem::obuf;
     uint32_t* xs = reinterpret_cast<uint32_t*>(wbase + WarpSmem::xs);
     int32_t* xr = reinterpret_cast<int32_t*>(wbase + WarpSmem::xr);
     int16_t* argr = reinterpret_cast<int16_t*>(wbase + WarpSmem::argr);
@@ -261,7 +259,6 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     // them before it writes argr, and clears them once it is done with argr.
     unsigned char* flg = wbase + WarpSmem::argr;
     uint64_t* fv = reinterpret_cast<uint64_t*>(wbase + WarpSmem::bars);
-    uint64_t* fo = fv + SW_NSV;
     T* out = static_cast<T*>(p.out);
     PartElem* tails = static_cast<PartElem*>(p.ws_parts);
     PartElem* heads = tails + U;
@@ -272,14 +269,10 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     const uint64_t obase = reinterpret_cast<uint64_t>(p.offsets);
     const Stream vs = make_stream(vbase, static_cast<uint64_t>(N) * 4, vbase + Ru * 4, vbase + Ru2 * 4,
                                   SW_VCHUNK);
-    const Stream os = make_stream(obase, static_cast<uint64_t>(S + 1) * OSZ, obase + Iu * OSZ,
-                                  obase + (Iu2 + 1) * OSZ, SW_OCHUNK);
     const int32_t nR = static_cast<int32_t>(Ru2 - Ru);
     // chunk 0's first row, relative to Ru (in [-3, 0]: chunks start 16-byte aligned)
     const int32_t cb0 = static_cast<int32_t>(static_cast<int64_t>(vs.A0 - vbase) / 4 - Ru);
     const uint64_t policy = policy_evict_first();
-    // ring byte of offsets entry Iu + i is (o_at0 + i * OSZ) mod SW_ORING
-    const uint32_t o_at0 = static_cast<uint32_t>(obase + static_cast<uint64_t>(Iu) * OSZ - os.A0);
 
     // Value chunk k into its stage (lane 0).  Chunks inside the buffer's
     // 16-byte-aligned interior take one bulk copy; the first and last may
@@ -308,7 +301,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     constexpr int kPrefetch = 2;   // value chunks prefetched into L2 beyond the staged ones
 
     if (lane == 0) {
-        for (int k = 0; k < SW_NSV + SW_NSO; ++k) mbar_init(&fv[k], 1);
+        for (int k = 0; k < SW_NSV; ++k) mbar_init(&fv[k], 1);
         fence_mbarrier_init();
     }
     // clear my flag bytes
@@ -317,39 +310,44 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     __syncwarp();
     // counters below are kept identical in every lane; lane 0 issues the copies
     int64_t v_issued = SW_NSV < vs.nch ? SW_NSV : vs.nch;
-    int64_t o_issued = SW_NSO < os.nch ? SW_NSO : os.nch;
     if (lane == 0) {
         for (int64_t k = 0; k < v_issued; ++k) issue_v(k);
         for (int k = 0; k < kPrefetch; ++k) prefetch_v(v_issued + k);
-        for (int64_t k = 0; k < o_issued; ++k)
-            issue_chunk(os, k, oring, SW_ORING, SW_OCHUNK, &fo[k % SW_NSO], policy);
     }
 
-    // offsets[Iu + i] from the ring, as a row relative to Ru clamped to
-    // [-1, nR + 1] (which also keeps malformed offsets inside the unit)
-    auto off_rel = [&](int64_t i) -> int32_t {
-        const uint32_t at = (o_at0 + static_cast<uint32_t>(i) * OSZ) & (SW_ORING - 1);
-        const int64_t x = static_cast<int64_t>(*reinterpret_cast<const OffT*>(oring + at)) - Ru;
+    // Segment ends: half `h` of the offsets buffer holds offsets[Iu + i0 + 1 ..
+    // Iu + i0 + n] for the tile that starts at end i0; lane l copies entries
+    // l, l + 32, ...
+    constexpr int NG = SW_EMAXT / 32;
+    auto load_ends = [&](int32_t i0, int n, int h) {
+        OffT* dst = reinterpret_cast<OffT*>(obuf) + h * SW_EMAXT;
+        const OffT* src = offs + Iu + i0 + 1;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            const int idx = 32 * g + lane;
+            if (idx < n) cp_async_small<OSZ>(dst + idx, src + idx);
+        }
+        cp_async_commit();
+    };
+    // an absolute offset as a row relative to Ru, clamped to [-1, nR + 1]
+    // (which also keeps malformed offsets inside the unit)
+    auto rel_off = [&](OffT raw) -> int32_t {
+        const int64_t x = static_cast<int64_t>(raw) - Ru;
         return static_cast<int32_t>(x < -1 ? -1 : (x > nR + 1 ? nR + 1 : x));
     };
-    int64_t ow = 0, odone = 0;   // offsets chunks waited for / handed back
     bool ok = true;
-    // wait until offsets entry Iu + i is in the ring
-    auto wait_offsets = [&](int64_t i) {
-        const int64_t need = static_cast<int64_t>((o_at0 + static_cast<uint64_t>(i + 1) * OSZ - 1) / SW_OCHUNK);
-        for (; ok && ow <= need && ow < os.nch; ++ow)
-            ok = wait_bounded(&fo[ow % SW_NSO], static_cast<uint32_t>((ow / SW_NSO) & 1), p.status,
-                              STATUS_CONSUMER_TIMEOUT);
-        ok = __all_sync(FULL, ok);
-    };
 
     C carry = CO::ident();
     const int64_t off_Iu = clamp_off(__ldg(&offs[Iu]), N);
     bool head_pending = (Iu < S) && off_Iu < Ru;
+    bool head_taken = false;                 // the head ticket was taken ...
+    unsigned long long head_ticket = 0;      // ... and returned this (lane 0)
     int64_t m = 0;            // current value chunk
     bool m_ready = false;
     int32_t ie = 0;           // next segment end, relative to Iu
     const int32_t nE = static_cast<int32_t>(Iu2 - Iu);
+    int oh = 0;               // offsets buffer half of the current tile
+    load_ends(0, nE < SW_EMAXT ? nE : SW_EMAXT, 0);
     int32_t b_es = off_Iu - Ru < -1 ? -1 : static_cast<int32_t>(off_Iu - Ru);   // offsets[Iu + ie]
     int32_t jj = 0;           // next row
 
@@ -365,14 +363,12 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
         }
         const int32_t rem = nE - ie;
         const int ncand = rem < SW_EMAXT ? rem : SW_EMAXT;
-        if (ncand > 0) {
-            wait_offsets(ie + ncand);
-            if (!ok) break;
-        }
         // This tile's ends: the prefix of the candidates whose segment ends by
         // row rl (all of them on the unit's last chunk).  Lane l keeps
         // E[g] = offsets[s + 1] of end s = Iu + ie + 32 g + l.
-        constexpr int NG = SW_EMAXT / 32;
+        cp_async_wait_all();
+        __syncwarp();
+        const OffT* ob_cur = reinterpret_cast<const OffT*>(obuf) + oh * SW_EMAXT;
         int32_t E[NG];
         int n_e = 0;
         bool more = true;
@@ -381,7 +377,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
             E[g] = INT32_MAX;
             if (more && 32 * g < ncand) {
                 const int idx = 32 * g + lane;
-                if (idx < ncand) E[g] = off_rel(ie + idx + 1);
+                if (idx < ncand) E[g] = rel_off(ob_cur[idx]);
                 const unsigned b = __ballot_sync(FULL, idx < ncand && (lastc || E[g] <= rl));
                 if (b != FULL) {
                     n_e += __ffs(~b) - 1;
@@ -393,6 +389,13 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
         }
         n_e = n_e < ncand ? n_e : ncand;
         const bool capped = n_e == SW_EMAXT && ie + n_e < nE;
+        if (n_e > 0) {
+            // the next tile's candidate ends go to the other half now
+            __syncwarp();
+            oh ^= 1;
+            const int32_t rem2 = nE - (ie + n_e);
+            load_ends(ie + n_e, rem2 < SW_EMAXT ? rem2 : SW_EMAXT, oh);
+        }
         // the segment left open after this tile starts at offsets[Iu + ie + n_e],
         // the E of the tile's last end
         int32_t elast = b_es;
@@ -550,30 +553,17 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
                 bool skip_first = false;
                 if (head_pending && n_e > 0) {
                     // end Iu began in an earlier unit: leave the head partial and
-                    // join the ticket (the whole warp takes part)
+                    // take the ticket; its answer is read when the unit is done
                     const int32_t oe = __shfl_sync(FULL, E[0], 0);
                     const bool rows_here = has_rows && oe - 1 >= jj;
                     const Acc<T> P = running_at(oe - 1 - cb, jr);
                     const C R = rows_here ? CO::then(carry, P) : carry;
-                    bool last = false;
-                    int pc = 0;
                     if (lane == 0) {
                         if constexpr (kFloatSum) heads[u_me] = to_part(R);
                         else heads[u_me] = to_part<T, OP>(R, Ru);
-                        __threadfence();
-                        pc = static_cast<int>((off_Iu - o0 + SW_CW * Iu) / Wu);
-                        pc = pc < 0 ? 0 : (pc > u_me ? static_cast<int>(u_me) : pc);
-                        last = ticket_arrive(p.ws_tickets, static_cast<int>(u_me),
-                                             static_cast<int>(u_me) - pc + 1, p.gen);
-                        if (last) __threadfence();
+                        head_ticket = ticket_take(p.ws_tickets, static_cast<int>(u_me), p.gen);
                     }
-                    last = __shfl_sync(FULL, last, 0);
-                    pc = __shfl_sync(FULL, pc, 0);
-                    if (last) {
-                        const int64_t oe1 = clamp_off(__ldg(&offs[Iu + 1]), N);
-                        warp_combine_store<T, OP>(p, tails, heads, pc, static_cast<int>(u_me), Iu,
-                                                  oe1 > off_Iu ? oe1 - off_Iu : 0, lane);
-                    }
+                    head_taken = true;
                     skip_first = true;   // lane 0 of the first group skips end Iu below
                 }
                 // the ends, 32 at a time: E = offsets[s + 1], B = offsets[s]
@@ -634,20 +624,6 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
             jj = tr1;
             ie += n_e;
             __syncwarp();
-            // hand back offsets chunks that hold only entries before Iu + ie
-            const int64_t keep_from = static_cast<int64_t>((o_at0 + static_cast<uint64_t>(ie) * OSZ) / SW_OCHUNK);
-            if (odone < keep_from && odone < ow) {
-                const int64_t upto = keep_from < ow ? keep_from : ow;
-                if (lane == 0) {
-                    for (int64_t k = odone; k < upto; ++k) {
-                        const int64_t nk = k + SW_NSO;
-                        if (nk < os.nch)
-                            issue_chunk(os, nk, oring, SW_ORING, SW_OCHUNK, &fo[nk % SW_NSO], policy);
-                    }
-                }
-                o_issued = upto + SW_NSO < os.nch ? upto + SW_NSO : os.nch;
-                odone = upto;
-            }
         }
         // The chunk is finished once its rows are done and no further end
         // falls in it (the tile was not cut short by the ends cap).
@@ -673,32 +649,51 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     }
 
     // ---- a6: the segment still open at the end of the unit -------------------------
+    // Its partial and ticket go out first; while that atomic is in flight the
+    // head ticket taken earlier is read, and its segment combined if this
+    // unit arrived last.
+    bool tail_taken = false;
+    unsigned long long tail_ticket = 0;
+    int tpc = 0, tqc = 0;
+    int64_t tob = 0;
     if (ok && Iu2 < S) {
-        const int64_t ob = clamp_off(__ldg(&offs[Iu2]), N);
-        if (ob < Ru2) {
-            bool last = false;
-            int pc = 0, qc = 0;
+        tob = clamp_off(__ldg(&offs[Iu2]), N);
+        if (tob < Ru2) {
             if (lane == 0) {
                 if constexpr (kFloatSum) tails[u_me] = to_part(carry);
                 else tails[u_me] = to_part<T, OP>(carry, Ru);
-                __threadfence();
                 const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
-                const int64_t f = ob - o0 + SW_CW * Iu2;
-                const int64_t e = (oe > ob ? oe : ob) - o0 + SW_CW * Iu2;
-                pc = static_cast<int>(f / Wu);
-                qc = static_cast<int>(e / Wu);
-                pc = pc < 0 ? 0 : (pc > u_me ? static_cast<int>(u_me) : pc);
-                qc = qc <= u_me ? static_cast<int>(u_me) + 1 : qc;
-                last = qc < U && ticket_arrive(p.ws_tickets, qc, qc - pc + 1, p.gen);
-                if (last) __threadfence();
+                const int64_t f = tob - o0 + SW_CW * Iu2;
+                const int64_t e = (oe > tob ? oe : tob) - o0 + SW_CW * Iu2;
+                tpc = static_cast<int>(f / Wu);
+                tqc = static_cast<int>(e / Wu);
+                tpc = tpc < 0 ? 0 : (tpc > u_me ? static_cast<int>(u_me) : tpc);
+                tqc = tqc <= u_me ? static_cast<int>(u_me) + 1 : tqc;
+                if (tqc < U) tail_ticket = ticket_take(p.ws_tickets, tqc, p.gen);
             }
-            last = __shfl_sync(FULL, last, 0);
-            pc = __shfl_sync(FULL, pc, 0);
-            qc = __shfl_sync(FULL, qc, 0);
-            if (last) {
-                const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
-                warp_combine_store<T, OP>(p, tails, heads, pc, qc, Iu2, oe > ob ? oe - ob : 0, lane);
-            }
+            tqc = __shfl_sync(FULL, tqc, 0);
+            tpc = __shfl_sync(FULL, tpc, 0);
+            tail_taken = tqc < U;
+        }
+    }
+    if (head_taken) {
+        int pc = static_cast<int>((off_Iu - o0 + SW_CW * Iu) / Wu);
+        pc = pc < 0 ? 0 : (pc > u_me ? static_cast<int>(u_me) : pc);
+        const bool last = __shfl_sync(
+            FULL, lane == 0 && ticket_last(head_ticket, p.gen, static_cast<int>(u_me) - pc + 1), 0);
+        if (last) {
+            fence_acq_rel_gpu();
+            const int64_t oe1 = clamp_off(__ldg(&offs[Iu + 1]), N);
+            warp_combine_store<T, OP>(p, tails, heads, pc, static_cast<int>(u_me), Iu,
+                                      oe1 > off_Iu ? oe1 - off_Iu : 0, lane);
+        }
+    }
+    if (tail_taken) {
+        const bool last = __shfl_sync(FULL, lane == 0 && ticket_last(tail_ticket, p.gen, tqc - tpc + 1), 0);
+        if (last) {
+            fence_acq_rel_gpu();
+            const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
+            warp_combine_store<T, OP>(p, tails, heads, tpc, tqc, Iu2, oe > tob ? oe - tob : 0, lane);
         }
     }
     // every copy this warp started must land before it exits
@@ -706,10 +701,8 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
         for (int64_t k = m + (m_ready ? 1 : 0); k < v_issued; ++k)
             wait_bounded(&fv[k % SW_NSV], static_cast<uint32_t>((k / SW_NSV) & 1), p.status,
                          STATUS_DRAIN_TIMEOUT);
-        for (int64_t k = ow; k < o_issued; ++k)
-            wait_bounded(&fo[k % SW_NSO], static_cast<uint32_t>((k / SW_NSO) & 1), p.status,
-                         STATUS_DRAIN_TIMEOUT);
     }
+    cp_async_wait_all();
 }
 
 }  // namespace segred
