@@ -302,6 +302,28 @@ __device__ __forceinline__ int64_t clamp_off(OffT raw, int64_t N) {
     return o > N ? N : o;
 }
 
+// At kernel start each CTA asks L2 for its 1/P slice of the offsets array
+// (when the array is small enough to stay there): the boundary search and the
+// units' own offsets loads then find it in L2 instead of each paying a DRAM
+// round trip.  The bytes are read once either way.
+constexpr uint64_t OFFSETS_PREFETCH_MAX = 32ull << 20;
+
+__device__ __forceinline__ void prefetch_offsets_slice(const void* offsets, uint64_t bytes, int cta, int P,
+                                                       int tid, int nth) {
+    if (bytes > OFFSETS_PREFETCH_MAX) return;
+    const uint64_t base = reinterpret_cast<uint64_t>(offsets);
+    const uint64_t ta = (base + 15) & ~uint64_t(15);
+    const uint64_t te = (base + bytes) & ~uint64_t(15);
+    if (te <= ta) return;
+    const uint64_t per = ((te - ta) / P + 4095) & ~uint64_t(4095);
+    const uint64_t a = ta + per * static_cast<uint64_t>(cta);
+    const uint64_t b = a + per < te ? a + per : te;
+    for (uint64_t c = a + static_cast<uint64_t>(tid) * 4096; c < b; c += static_cast<uint64_t>(nth) * 4096) {
+        const uint64_t e = c + 4096 < b ? c + 4096 : b;
+        bulk_prefetch_l2(reinterpret_cast<const void*>(c), static_cast<uint32_t>(e - c));
+    }
+}
+
 // Cross-unit arrival for the segment whose end lies in unit q, in two halves
 // so that the caller can go on working while the atomic is in flight.
 // Tickets carry the call generation in the high half: a stale count left by

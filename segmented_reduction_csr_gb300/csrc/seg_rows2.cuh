@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     // the I(D) = #{s : key(s) < D} ends before it and the rows before both
     // D - RW_CW I and the start of segment I.
     RowsSearchSmem* ss = reinterpret_cast<RowsSearchSmem*>(smem);
+    prefetch_offsets_slice(p.offsets, static_cast<uint64_t>(S + 1) * sizeof(OffT), cta, p.P, tid, RW_NTHREADS);
     if (tid == 0) ss->o0 = clamp_off(__ldg(&offs[0]), N);
     if (tid == 1) ss->oS = clamp_off(__ldg(&offs[S]), N);
     for (int m = tid; m < RW_GRID; m += RW_NTHREADS) {

@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     // fixed grid of SW_GRID keys that every CTA shares (so it hits L2); then
     // each boundary narrows its bracket with SW_PROBES probes per round.
     SearchSmem* ss = reinterpret_cast<SearchSmem*>(smem);
+    prefetch_offsets_slice(p.offsets, static_cast<uint64_t>(S + 1) * OSZ, cta, p.P, tid, SW_NTHREADS);
     if (tid == 0) ss->o0 = clamp_off(__ldg(&offs[0]), N);
     if (tid == 1) ss->oS = clamp_off(__ldg(&offs[S]), N);
     for (int m = tid; m < SW_GRID; m += SW_NTHREADS) {
@@ -339,6 +340,10 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
 
     C carry = CO::ident();
     const int64_t off_Iu = clamp_off(__ldg(&offs[Iu]), N);
+    // offsets the unit's head and tail need at the end, loaded now
+    const int64_t off_Iu1 = Iu < S ? clamp_off(__ldg(&offs[Iu + 1]), N) : 0;
+    const int64_t off_Iu2 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2]), N) : 0;
+    const int64_t off_Iu21 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2 + 1]), N) : 0;
     bool head_pending = (Iu < S) && off_Iu < Ru;
     bool head_taken = false;                 // the head ticket was taken ...
     unsigned long long head_ticket = 0;      // ... and returned this (lane 0)
@@ -657,12 +662,12 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     int tpc = 0, tqc = 0;
     int64_t tob = 0;
     if (ok && Iu2 < S) {
-        tob = clamp_off(__ldg(&offs[Iu2]), N);
+        tob = off_Iu2;
         if (tob < Ru2) {
             if (lane == 0) {
                 if constexpr (kFloatSum) tails[u_me] = to_part(carry);
                 else tails[u_me] = to_part<T, OP>(carry, Ru);
-                const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
+                const int64_t oe = off_Iu21;
                 const int64_t f = tob - o0 + SW_CW * Iu2;
                 const int64_t e = (oe > tob ? oe : tob) - o0 + SW_CW * Iu2;
                 tpc = static_cast<int>(f / Wu);
@@ -683,17 +688,15 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
             FULL, lane == 0 && ticket_last(head_ticket, p.gen, static_cast<int>(u_me) - pc + 1), 0);
         if (last) {
             fence_acq_rel_gpu();
-            const int64_t oe1 = clamp_off(__ldg(&offs[Iu + 1]), N);
             warp_combine_store<T, OP>(p, tails, heads, pc, static_cast<int>(u_me), Iu,
-                                      oe1 > off_Iu ? oe1 - off_Iu : 0, lane);
+                                      off_Iu1 > off_Iu ? off_Iu1 - off_Iu : 0, lane);
         }
     }
     if (tail_taken) {
         const bool last = __shfl_sync(FULL, lane == 0 && ticket_last(tail_ticket, p.gen, tqc - tpc + 1), 0);
         if (last) {
             fence_acq_rel_gpu();
-            const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
-            warp_combine_store<T, OP>(p, tails, heads, tpc, tqc, Iu2, oe > tob ? oe - tob : 0, lane);
+            warp_combine_store<T, OP>(p, tails, heads, tpc, tqc, Iu2, off_Iu21 > tob ? off_Iu21 - tob : 0, lane);
         }
     }
     // every copy this warp started must land before it exits
