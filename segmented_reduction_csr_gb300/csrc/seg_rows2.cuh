@@ -35,6 +35,7 @@ constexpr int RW_NDIAG = RW_NW + 1;           // range boundaries per CTA (at mo
 constexpr int RW_GRID = 1024;                 // first-round probes, shared by all CTAs
 constexpr int RW_PROBES = 56;                 // later-round probes per boundary
 constexpr int RW_MIN_ITEMS = 128;             // weighted items per range, at least
+constexpr int64_t RW_ADOPT = 512;             // rows of a cut-crossing segment a range adopts
 constexpr int RW_NSR = 3;                     // staged rows: shared-memory stages per warp
 constexpr uint32_t RW_CB = 8192;              // staged rows: bytes per stage
 static_assert(RW_NDIAG * RW_PROBES <= 2 * RW_NTHREADS, "two probes per thread per round");
@@ -251,10 +252,29 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     const int64_t Dlo = ss->D[bi], Dhi = ss->D[bi + 1];
     const int64_t Iu = ss->lo[bi];
     const int64_t Iu2 = ss->lo[bi + 1] > Iu ? ss->lo[bi + 1] : Iu;
-    const int64_t Ru = ss->R[bi];
-    const int64_t Ru2 = ss->R[bi + 1] > Ru ? ss->R[bi + 1] : Ru;
+    const int64_t Rc = ss->R[bi];                           // the cuts' rows
+    const int64_t Rc2 = ss->R[bi + 1] > Rc ? ss->R[bi + 1] : Rc;
     __syncthreads();   // the search scratch is dead from here on (staged rows reuse it)
     if (rg >= NR || Dlo >= Dhi) return;
+    // Offsets of the segment that crosses each cut, and adoption: a segment
+    // that crosses just one cut with at most RW_ADOPT rows before it is taken
+    // whole by the range that holds its end (which starts at the segment's
+    // first row; the range before it stops there), so it needs no partial
+    // and no ticket.  Both sides decide it from the same cut and offsets.
+    const int64_t off_Iu = clamp_off(__ldg(&offs[Iu]), N);
+    const int64_t off_Iu1 = Iu < S ? clamp_off(__ldg(&offs[Iu + 1]), N) : 0;
+    const int64_t off_Iu2 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2]), N) : 0;
+    const int64_t off_Iu21 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2 + 1]), N) : 0;
+    bool adopt_head = false, give_tail = false;
+    if (Iu < Iu2 && off_Iu < Rc && Rc - off_Iu <= RW_ADOPT && rg > 0)
+        adopt_head = (off_Iu - o0 + RW_CW * Iu) / Wr == rg - 1;
+    if (Iu2 < S && off_Iu2 < Rc2 && Rc2 - off_Iu2 <= RW_ADOPT) {
+        const int64_t f = off_Iu2 - o0 + RW_CW * Iu2;
+        const int64_t e = (off_Iu21 > off_Iu2 ? off_Iu21 : off_Iu2) - o0 + RW_CW * Iu2;
+        give_tail = f / Wr == rg && e / Wr == rg + 1;
+    }
+    const int64_t Ru = adopt_head ? off_Iu : Rc;
+    const int64_t Ru2 = give_tail ? (off_Iu2 > Ru ? off_Iu2 : Ru) : Rc2;
 
     // ---- per-warp state ----------------------------------------------------------
     const int c0 = slice * SLW + lane * VEC;   // my first column
@@ -290,7 +310,6 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     int k = 0;
     int32_t ecur = __shfl_sync(FULL, EB, 0);
     int64_t s = Iu;
-    const int64_t off_Iu = clamp_off(__ldg(&offs[Iu]), N);
     bool head_pending = Iu < S && off_Iu < Ru;
     int32_t bst = rel(off_Iu);   // start of segment s
 
@@ -567,13 +586,13 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     unsigned long long tail_ticket = 0;
     int64_t tpc = 0, tqc = 0, tob = 0;
     if (Iu2 < S) {
-        tob = clamp_off(__ldg(&offs[Iu2]), N);
+        tob = off_Iu2;
         if (tob < Ru2) {
             write_part(u_me);
             __threadfence();
             __syncwarp();   // every lane's partial is out before the ticket
             if (lane == 0) {
-                const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
+                const int64_t oe = off_Iu21;
                 const int64_t f = tob - o0 + RW_CW * Iu2;
                 const int64_t e = (oe > tob ? oe : tob) - o0 + RW_CW * Iu2;
                 tpc = f / Wr;
@@ -594,9 +613,8 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
             __shfl_sync(FULL, lane == 0 && ticket_last(head_ticket, p.gen, static_cast<int>(rg - pc + 1)), 0);
         if (last) {
             fence_acq_rel_gpu();
-            const int64_t oe1 = clamp_off(__ldg(&offs[Iu + 1]), N);
-            rows_combine_store<T, OP, VEC>(p, pv, pr, U, NSL, slice, pc, rg, Iu, oe1 > off_Iu ? oe1 - off_Iu : 0,
-                                           lane);
+            rows_combine_store<T, OP, VEC>(p, pv, pr, U, NSL, slice, pc, rg, Iu,
+                                           off_Iu1 > off_Iu ? off_Iu1 - off_Iu : 0, lane);
         }
     }
     if (tail_taken) {
@@ -604,8 +622,8 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
             __shfl_sync(FULL, lane == 0 && ticket_last(tail_ticket, p.gen, static_cast<int>(tqc - tpc + 1)), 0);
         if (last) {
             fence_acq_rel_gpu();
-            const int64_t oe = clamp_off(__ldg(&offs[Iu2 + 1]), N);
-            rows_combine_store<T, OP, VEC>(p, pv, pr, U, NSL, slice, tpc, tqc, Iu2, oe > tob ? oe - tob : 0, lane);
+            rows_combine_store<T, OP, VEC>(p, pv, pr, U, NSL, slice, tpc, tqc, Iu2,
+                                           off_Iu21 > tob ? off_Iu21 - tob : 0, lane);
         }
     }
 }

@@ -54,6 +54,7 @@ constexpr int SW_TROWS = 32 * SW_KR;           // rows per value chunk
 constexpr uint32_t SW_VCHUNK = SW_TROWS * 4;   // bytes per value chunk
 constexpr int SW_NSV = 2;                      // value stages per warp
 constexpr int SW_EMAXT = 160;                  // segment ends per tile
+constexpr int64_t SW_ADOPT = 1152;             // rows of a cut-crossing segment a unit adopts
 constexpr int SW_NDIAG = SW_NW + 1;            // unit boundaries per CTA
 constexpr int SW_GRID = 1024;                  // first-round probes, shared by all CTAs
 constexpr int SW_PROBES = 60;                  // later-round probes per boundary
@@ -244,10 +245,31 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     const int64_t Dlo = ss->D[warp], Dhi = ss->D[warp + 1];
     const int64_t Iu = ss->lo[warp];
     const int64_t Iu2 = ss->lo[warp + 1] > Iu ? ss->lo[warp + 1] : Iu;
-    const int64_t Ru = ss->R[warp];
-    const int64_t Ru2 = ss->R[warp + 1] > Ru ? ss->R[warp + 1] : Ru;
+    const int64_t Rc = ss->R[warp];                              // the cuts' rows
+    const int64_t Rc2 = ss->R[warp + 1] > Rc ? ss->R[warp + 1] : Rc;
     __syncthreads();   // the search scratch is dead from here on
     if (Dlo >= Dhi) return;
+    // Offsets of the segment that crosses each cut (loaded now; the head and
+    // tail logic needs them).
+    const int64_t off_Iu = clamp_off(__ldg(&offs[Iu]), N);
+    const int64_t off_Iu1 = Iu < S ? clamp_off(__ldg(&offs[Iu + 1]), N) : 0;
+    const int64_t off_Iu2 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2]), N) : 0;
+    const int64_t off_Iu21 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2 + 1]), N) : 0;
+    // A segment that crosses just one cut, with at most SW_ADOPT rows before
+    // it, is adopted whole by the unit that holds its end: that unit starts
+    // at the segment's first row and the unit before it stops there, so no
+    // partial and no ticket are needed.  Both sides decide it from the same
+    // cut and the same offsets.
+    bool adopt_head = false, give_tail = false;
+    if (Iu < Iu2 && off_Iu < Rc && Rc - off_Iu <= SW_ADOPT && u_me > 0)
+        adopt_head = (off_Iu - o0 + SW_CW * Iu) / Wu == u_me - 1;
+    if (Iu2 < S && off_Iu2 < Rc2 && Rc2 - off_Iu2 <= SW_ADOPT) {
+        const int64_t f = off_Iu2 - o0 + SW_CW * Iu2;
+        const int64_t e = (off_Iu21 > off_Iu2 ? off_Iu21 : off_Iu2) - o0 + SW_CW * Iu2;
+        give_tail = f / Wu == u_me && e / Wu == u_me + 1;
+    }
+    const int64_t Ru = adopt_head ? off_Iu : Rc;
+    const int64_t Ru2 = give_tail ? (off_Iu2 > Ru ? off_Iu2 : Ru) : Rc2;
 
     // ---- per-warp state ----------------------------------------------------------
     unsigned char* wbase = smem + warp * WarpSmem::bytes;
@@ -339,11 +361,6 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     bool ok = true;
 
     C carry = CO::ident();
-    const int64_t off_Iu = clamp_off(__ldg(&offs[Iu]), N);
-    // offsets the unit's head and tail need at the end, loaded now
-    const int64_t off_Iu1 = Iu < S ? clamp_off(__ldg(&offs[Iu + 1]), N) : 0;
-    const int64_t off_Iu2 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2]), N) : 0;
-    const int64_t off_Iu21 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2 + 1]), N) : 0;
     bool head_pending = (Iu < S) && off_Iu < Ru;
     bool head_taken = false;                 // the head ticket was taken ...
     unsigned long long head_ticket = 0;      // ... and returned this (lane 0)
