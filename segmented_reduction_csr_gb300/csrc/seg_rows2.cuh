@@ -87,23 +87,40 @@ __device__ __forceinline__ void rows_combine_store(const Params& p, const uint32
         tv[v] = T(0);
         trow[v] = -1;
     }
-#pragma unroll 4
-    for (int64_t k = pc; k <= qc; ++k) {
-        const int64_t unit = (k < qc ? 0 : U) + k * NSL + slice;
-        const int64_t at = unit * SLW + lane * VEC;
+    // Partials are read KB units at a time (all loads of a batch in flight
+    // together: a long segment has hundreds of them) and folded in order.
+    constexpr int KB = OP == OP_SUM ? 16 : 8;
+    for (int64_t k0 = pc; k0 <= qc; k0 += KB) {
+        uint32_t b[KB][VEC];
+        int64_t rr[OP == OP_SUM ? 1 : KB][VEC];
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            const uint32_t b = __ldcg(&pv[at + v]);
-            if constexpr (OP == OP_SUM) {
-                if constexpr (kIsFloat<T>) ds[v] += static_cast<double>(__uint_as_float(b));
-                else tv[v] = add_wrap(tv[v], from_bits<T>(b));
-            } else {
-                const int64_t r = __ldcg(&pr[at + v]);
-                const T x = from_bits<T>(b);
-                const bool better = (OP == OP_MIN) ? (x < tv[v]) : (x > tv[v]);
-                if (r >= 0 && (trow[v] < 0 || better)) {
-                    tv[v] = x;
-                    trow[v] = r;
+        for (int j = 0; j < KB; ++j) {
+            const int64_t k = k0 + j;
+            if (k <= qc) {
+                const int64_t at = ((k < qc ? 0 : U) + k * NSL + slice) * SLW + lane * VEC;
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    b[j][v] = __ldcg(&pv[at + v]);
+                    if constexpr (OP != OP_SUM) rr[j][v] = __ldcg(&pr[at + v]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < KB; ++j) {
+            if (k0 + j <= qc) {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    if constexpr (OP == OP_SUM) {
+                        if constexpr (kIsFloat<T>) ds[v] += static_cast<double>(__uint_as_float(b[j][v]));
+                        else tv[v] = add_wrap(tv[v], from_bits<T>(b[j][v]));
+                    } else {
+                        const T x = from_bits<T>(b[j][v]);
+                        const bool better = (OP == OP_MIN) ? (x < tv[v]) : (x > tv[v]);
+                        if (rr[j][v] >= 0 && (trow[v] < 0 || better)) {
+                            tv[v] = x;
+                            trow[v] = rr[j][v];
+                        }
+                    }
                 }
             }
         }

@@ -47,7 +47,7 @@ namespace segred {
 
 constexpr int SW_NW = 16;                      // warps (units) per CTA
 constexpr int SW_NTHREADS = SW_NW * 32;
-constexpr int SW_CW = 4;                       // merge-path weight of a segment end, in rows
+constexpr int SW_CW = 24;                      // merge-path weight of a segment end, in rows
 constexpr int SW_KR = 36;                      // rows per lane per tile
 constexpr int SW_Q = SW_KR / 4;                // quads per lane
 constexpr int SW_TROWS = 32 * SW_KR;           // rows per value chunk
