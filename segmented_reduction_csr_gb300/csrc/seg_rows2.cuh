@@ -460,7 +460,8 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
         // Rows of 16-byte multiples, one column slice: the range is one
         // contiguous byte run, streamed in chunks of RPC whole rows through
         // RW_NSR stages of this warp's shared memory by 1-D bulk copies (lane
-        // 0 issues; the chunk two beyond the staged ones is prefetched into L2).
+        // 0 issues).  An L2 prefetch further ahead measured slower here: the
+        // copies already keep enough bytes in flight.
         const uint32_t rowb = static_cast<uint32_t>(F) * 4;
         const int32_t RPC = static_cast<int32_t>(RW_CB / rowb);
         unsigned char* ring = smem + warp * (RW_NSR * RW_CB);
@@ -479,16 +480,10 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
             bulk_load(ring + (k % RW_NSR) * RW_CB, reinterpret_cast<const void*>(src0 + k * RPC * rowb), nb, bar,
                       pol);
         };
-        auto prefetch = [&](int64_t k) {   // lane 0
-            if (k < nch)
-                bulk_prefetch_l2(reinterpret_cast<const void*>(src0 + k * RPC * rowb), chunk_bytes(k));
-        };
         if (lane == 0) {
             for (int k = 0; k < RW_NSR; ++k) mbar_init(&bars[k], 1);
             fence_mbarrier_init();
             for (int64_t k = 0; k < RW_NSR && k < nch; ++k) issue(k);
-            prefetch(RW_NSR);
-            prefetch(RW_NSR + 1);
         }
         __syncwarp();
         int64_t k = 0;
@@ -532,10 +527,7 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
                 fold_block();
             }
             __syncwarp();   // every lane is done with the stage before it is refilled
-            if (lane == 0 && k + RW_NSR < nch) {
-                issue(k + RW_NSR);
-                prefetch(k + RW_NSR + 2);
-            }
+            if (lane == 0 && k + RW_NSR < nch) issue(k + RW_NSR);
         }
         if (!ok) {
             // a wait ran out (recorded in the status word): let every copy land, then stop

@@ -10,8 +10,7 @@
 // runs on its own: no CTA barrier in the main loop.
 //
 // Per warp.  Lane 0 streams the unit's rows (SW_VCHUNK-byte chunks, SW_NSV
-// stages, with the next chunks prefetched into L2 so that a refill finds them
-// there) into the warp's shared memory with 1-D bulk copies, refilling a
+// stages) into the warp's shared memory with 1-D bulk copies, refilling a
 // stage as soon as the warp is done with it.  The segment ends of the next
 // tile are copied by every lane (per-thread async copies, one entry each)
 // into the other half of a double buffer while the current tile runs.
@@ -311,17 +310,6 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
             issue_chunk_to(vs, k, SW_VCHUNK, dst, bar, policy);
         }
     };
-    // L2 prefetch of the interior bytes of value chunk k (lane 0)
-    auto prefetch_v = [&](int64_t k) {
-        if (k >= vs.nch) return;
-        const uint64_t cs = vs.A0 + static_cast<uint64_t>(k) * SW_VCHUNK;
-        uint64_t ce = cs + SW_VCHUNK;
-        ce = ce < vs.AE ? ce : vs.AE;
-        ce = ce < vs.TE ? ce : vs.TE;
-        const uint64_t c0 = cs > vs.TA ? cs : vs.TA;
-        if (ce > c0) bulk_prefetch_l2(reinterpret_cast<const void*>(c0), static_cast<uint32_t>(ce - c0));
-    };
-    constexpr int kPrefetch = 2;   // value chunks prefetched into L2 beyond the staged ones
 
     if (lane == 0) {
         for (int k = 0; k < SW_NSV; ++k) mbar_init(&fv[k], 1);
@@ -335,7 +323,6 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     int64_t v_issued = SW_NSV < vs.nch ? SW_NSV : vs.nch;
     if (lane == 0) {
         for (int64_t k = 0; k < v_issued; ++k) issue_v(k);
-        for (int k = 0; k < kPrefetch; ++k) prefetch_v(v_issued + k);
     }
 
     // Segment ends: half `h` of the offsets buffer holds offsets[Iu + i0 + 1 ..
@@ -659,10 +646,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
             fence_proxy_async_smem();
             __syncwarp();
             if (v_issued < vs.nch) {
-                if (lane == 0) {
-                    issue_v(v_issued);
-                    prefetch_v(v_issued + kPrefetch);
-                }
+                if (lane == 0) issue_v(v_issued);
                 ++v_issued;
             }
             ++m;
