@@ -341,9 +341,12 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     };
     // an absolute offset as a row relative to Ru, clamped to [-1, nR + 1]
     // (which also keeps malformed offsets inside the unit)
+    // (in 32 bits: a unit spans fewer than 2^31 rows, so a valid offset is
+    // exact; a malformed one wraps, and the clamp still keeps it in the unit)
+    const uint32_t Ru_lo = static_cast<uint32_t>(Ru);
     auto rel_off = [&](OffT raw) -> int32_t {
-        const int64_t x = static_cast<int64_t>(raw) - Ru;
-        return static_cast<int32_t>(x < -1 ? -1 : (x > nR + 1 ? nR + 1 : x));
+        const int32_t x = static_cast<int32_t>(static_cast<uint32_t>(raw) - Ru_lo);
+        return x < -1 ? -1 : (x > nR + 1 ? nR + 1 : x);
     };
     bool ok = true;
 
@@ -374,7 +377,9 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
         const int ncand = rem < SW_EMAXT ? rem : SW_EMAXT;
         // This tile's ends: the prefix of the candidates whose segment ends by
         // row rl (all of them on the unit's last chunk).  Lane l keeps
-        // E[g] = offsets[s + 1] of end s = Iu + ie + 32 g + l.
+        // E[g] = offsets[s + 1] of end s = Iu + ie + 32 g + l.  The same pass
+        // sets the start flag of each row inside the chunk where a segment
+        // starts (for valid offsets those are exactly this tile's ends).
         cp_async_wait_all();
         __syncwarp();
         const OffT* ob_cur = reinterpret_cast<const OffT*>(obuf) + oh * SW_EMAXT;
@@ -387,6 +392,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
             if (more && 32 * g < ncand) {
                 const int idx = 32 * g + lane;
                 if (idx < ncand) E[g] = rel_off(ob_cur[idx]);
+                if (E[g] >= jj && E[g] < rl && m < vs.nch) flg[E[g] - cb] = 1;
                 const unsigned b = __ballot_sync(FULL, idx < ncand && (lastc || E[g] <= rl));
                 if (b != FULL) {
                     n_e += __ffs(~b) - 1;
@@ -449,13 +455,8 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
                 carry = b_es < jj ? CO::then(carry, a) : CO::from(a);
             } else {
                 if (has_rows) {
-                    // start flags: the tile's first row and, for each end, the
-                    // row where the next segment starts
+                    // start flags: the tile's first row (the ends' were set above)
                     if (lane == 0) flg[jr] = 1;
-#pragma unroll
-                    for (int g = 0; g < NG; ++g) {
-                        if (32 * g + lane < n_e && E[g] >= jj && E[g] < tr1) flg[E[g] - cb] = 1;
-                    }
                     __syncwarp();
                     uint32_t fw[SW_Q];
 #pragma unroll
@@ -576,6 +577,8 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
                     skip_first = true;   // lane 0 of the first group skips end Iu below
                 }
                 // the ends, 32 at a time: E = offsets[s + 1], B = offsets[s]
+                T* const out_t = out + (Iu + ie);
+                int64_t* const arg_t = want_arg ? p.out_arg + (Iu + ie) : nullptr;
                 int32_t prevE = b_es;
 #pragma unroll
                 for (int g = 0; g < NG; ++g) {
@@ -587,7 +590,6 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
                         const int32_t ob = lane == 0 ? prevE : up;
                         prevE = __shfl_sync(FULL, oe, 31);
                         if (valid) {
-                            const int64_t s = Iu + ie + idx;
                             const int32_t len = oe > ob ? oe - ob : 0;
                             T v;
                             int64_t a;
@@ -606,8 +608,8 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
                                     finish_acc<T, OP>(R, len, mean, Ru, v, a);
                                 }
                             }
-                            out[s] = v;
-                            if (want_arg) p.out_arg[s] = a;
+                            out_t[idx] = v;
+                            if (want_arg) arg_t[idx] = a;
                         }
                     }
                 }
