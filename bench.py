@@ -127,6 +127,43 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---- ranks: one process per GPU under torchrun, each an independent replica ---------
+def dist_init(backend: str, device=None):
+    """(world, rank) from the torchrun environment; joins the process group when world > 1."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            if device is not None:
+                dist.init_process_group(backend, device_id=device)
+            else:
+                dist.init_process_group(backend)
+    return world, rank
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest x over all ranks (a timing: the job ends with its slowest rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, bytes_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank moves bytes_per_step per step (weak scaling)."""
+    return world * bytes_per_step * steps / (ms * 1e-3) / 1e9
+
+
 def cases_of(w: W.Workload):
     return [(k, op) for k, op in w.cases]
 
@@ -201,14 +238,10 @@ def run_ours(args, w: W.Workload):
     import segmented_reduction_csr_gb300 as sr
     from segmented_reduction_csr_gb300 import build as srbuild
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    world, rank = dist_init("nccl", dev)
     torch.cuda.set_device(dev)
     srbuild.build()
     lib = sr.load_library()
@@ -247,8 +280,7 @@ def run_ours(args, w: W.Workload):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps * len(cases))]
     clocks = ClockSampler(local)
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)
@@ -265,14 +297,10 @@ def run_ours(args, w: W.Workload):
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
     per_call = [s.elapsed_time(e) for s, e in ev]             # ms
-    kernel_ms = sum(per_call)
-    if world > 1:
-        t = torch.tensor([kernel_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        kernel_ms = float(t.item())
+    kernel_ms = max_over_ranks(sum(per_call), world, dev)
     assert sr.device_status(stream) == 0
     bytes_step = step_bytes(w)
-    value = world * bytes_step * args.steps / (kernel_ms * 1e-3) / 1e9
+    value = whole_job_gbs(world, bytes_step, args.steps, kernel_ms)
     by_case = {}
     for idx, (k, op) in enumerate(cases * args.steps):
         by_case.setdefault((k, op), []).append(per_call[idx])
@@ -316,12 +344,8 @@ def run_ours(args, w: W.Workload):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = world * bytes_step * args.steps / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_val = whole_job_gbs(world, bytes_step, args.steps, e2e_ms)
 
     # ---- CPU baseline (rank 0, N == 1 only) --------------------------------
     cpu = None
