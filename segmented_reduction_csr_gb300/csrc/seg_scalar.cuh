@@ -404,6 +404,10 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
         }
         n_e = n_e < ncand ? n_e : ncand;
         const bool capped = n_e == SW_EMAXT && ie + n_e < nE;
+        // the segment left open after this tile starts at offsets[Iu + ie + n_e],
+        // the E of the tile's last end (read back from the buffer: selecting it
+        // from E[] would index the array at run time)
+        const int32_t bo = n_e == 0 ? b_es : rel_off(ob_cur[n_e - 1]);
         if (n_e > 0) {
             // the next tile's candidate ends go to the other half now
             __syncwarp();
@@ -411,13 +415,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
             const int32_t rem2 = nE - (ie + n_e);
             load_ends(ie + n_e, rem2 < SW_EMAXT ? rem2 : SW_EMAXT, oh);
         }
-        // the segment left open after this tile starts at offsets[Iu + ie + n_e],
-        // the E of the tile's last end
-        int32_t elast = b_es;
-#pragma unroll
-        for (int g = 0; g < NG; ++g)
-            if (((n_e - 1) >> 5) == g) elast = E[g];
-        const int32_t bo = n_e == 0 ? b_es : __shfl_sync(FULL, elast, (n_e - 1) & 31);
+
         const int32_t tr1 = capped ? (bo < jj ? jj : (bo > rl ? rl : bo)) : rl;
 
         // ---- one tile: rows [jj, tr1) of chunk m, ends [ie, ie + n_e) ---------------
@@ -469,6 +467,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
                     }
                     // inclusive segmented scan of my rows, a quad at a time
                     const int32_t hi = tr - lrow0;        // my rows below tr1
+                    const bool full_tail = tr == SW_TROWS;    // the same in every lane
                     Acc<T> acc = RD::ident();
                     bool fi = false;
 #pragma unroll
@@ -495,8 +494,9 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
                             xb[t] = bits_of(acc.v);
                         }
                         // running values back over rows < tr1 (later rows are the
-                        // next tile's input; earlier rows are finished)
-                        if (4 * q + 4 <= hi) {
+                        // next tile's input; earlier rows are finished); a tile
+                        // that runs to the chunk's end writes every quad
+                        if (full_tail || 4 * q + 4 <= hi) {
                             *reinterpret_cast<uint4*>(mine + 16 * q) = make_uint4(xb[0], xb[1], xb[2], xb[3]);
                             if constexpr (OP != OP_SUM)
                                 *reinterpret_cast<uint2*>(&argr[lrow0 + 4 * q]) = make_uint2(
