@@ -11,6 +11,9 @@ Two independent implementations live here:
   synthetic workloads.
 * ``brute.seg_reduce``: a pure-Python restatement with Python integers and
   ``math.fsum`` for tiny inputs, used to pin the C oracle.
+* ``rle`` / ``flags_to_offsets``: the sequential C loops in ``rle_oracle.c``
+  for the producers of offsets (GPURunLengthEncode / GPUUnique,
+  GPUSegmentedLayout), pinned by ``brute.rle`` / ``brute.flags_to_offsets``.
 
 Semantics (GPUSegmentedReduction "Contract"; graph-reduce README "API",
 "Method" and "Correctness"): segment ``s`` reduces rows
@@ -32,6 +35,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "seg_oracle.c")
 _LIBDIR = os.path.join(_HERE, "lib")
 _LIB = os.path.join(_LIBDIR, "libsegoracle.so")
+_RLE_SRC = os.path.join(_HERE, "rle_oracle.c")
+_RLE_LIB = os.path.join(_LIBDIR, "libsegrleoracle.so")
 
 # Codes private to seg_oracle.c.
 _DT = {np.dtype(np.uint32): 0, np.dtype(np.int32): 1, np.dtype(np.float32): 2}
@@ -55,12 +60,13 @@ def compile_source(src: str, dst: str) -> str:
 
 
 def build(force: bool = False) -> str:
-    """Compile seg_oracle.c into lib/libsegoracle.so."""
+    """Compile seg_oracle.c into lib/libsegoracle.so and rle_oracle.c into
+    lib/libsegrleoracle.so."""
     os.makedirs(_LIBDIR, exist_ok=True)
-    if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
-        return _LIB
-    return compile_source(_SRC, _LIB)
+    for src, lib in ((_RLE_SRC, _RLE_LIB), (_SRC, _LIB)):
+        if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(src):
+            compile_source(src, lib)
+    return _LIB
 
 
 def load_library(path: str):
@@ -117,3 +123,55 @@ def seg_reduce(values, offsets, op: str, with_arg: bool = True, lib=None):
         raise ValueError(f"oracle rejected the input: {_ERR.get(rc, rc)}")
     return (out, arg) if want_arg else out
 
+
+
+_rle_lib = None
+
+
+def load_rle_library(path: str):
+    """ctypes handle of a compiled RLE oracle library (the default one, or a
+    deliberately broken copy that a test builds to check the pins)."""
+    lib = ctypes.CDLL(path)
+    lib.oracle_rle.restype = ctypes.c_int64
+    lib.oracle_rle.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                               ctypes.c_void_p]
+    lib.oracle_flags_to_offsets.restype = ctypes.c_int64
+    lib.oracle_flags_to_offsets.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    return lib
+
+
+def _load_rle():
+    global _rle_lib
+    with _lock:
+        if _rle_lib is None:
+            build()
+            _rle_lib = load_rle_library(_RLE_LIB)
+    return _rle_lib
+
+
+def rle(keys, lib=None):
+    """Run-length encoding of an ordered uint32 vector: ``(values, lengths,
+    offsets)`` with ``offsets`` one longer (run starts, then n)."""
+    keys = np.ascontiguousarray(keys, dtype=np.uint32)
+    n = keys.shape[0]
+    values = np.zeros(n, np.uint32)
+    lengths = np.zeros(n, np.uint32)
+    offsets = np.zeros(n + 1, np.int64)
+    lib = _load_rle() if lib is None else lib
+    runs = lib.oracle_rle(keys.ctypes.data if n else None, n, values.ctypes.data, lengths.ctypes.data,
+                          offsets.ctypes.data)
+    if runs < 0:
+        raise ValueError("oracle rejected the input")
+    return values[:runs].copy(), lengths[:runs].copy(), offsets[: runs + 1].copy()
+
+
+def flags_to_offsets(flags, lib=None):
+    """Offsets from segment-start flags: the indices of the non-zero flags, then n."""
+    flags = np.ascontiguousarray(flags, dtype=np.uint8)
+    n = flags.shape[0]
+    offsets = np.zeros(n + 1, np.int64)
+    lib = _load_rle() if lib is None else lib
+    count = lib.oracle_flags_to_offsets(flags.ctypes.data if n else None, n, offsets.ctypes.data)
+    if count < 0:
+        raise ValueError("oracle rejected the input")
+    return offsets[: count + 1].copy()

@@ -64,3 +64,25 @@ def seg_reduce(values, offsets, op: str, kind: str, feat=None):
         out.append(orow)
         arg.append(arow)
     return out, arg
+
+
+def rle(keys):
+    """Runs of adjacent equal values by itertools.groupby (GPURunLengthEncode,
+    "What is run-length encoding?"): (values, lengths, offsets)."""
+    import itertools
+    values, lengths, offsets = [], [], []
+    pos = 0
+    for key, grp in itertools.groupby(list(keys)):
+        k = len(list(grp))
+        values.append(key)
+        lengths.append(k)
+        offsets.append(pos)
+        pos += k
+    offsets.append(pos)
+    return values, lengths, offsets
+
+
+def flags_to_offsets(flags):
+    """The indices whose flag is set, then the length (GPUSegmentedLayout)."""
+    flags = list(flags)
+    return [i for i, f in enumerate(flags) if f] + [len(flags)]
