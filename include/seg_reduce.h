@@ -200,6 +200,64 @@ seg_status_t seg_reduce_noalloc(const void *values, seg_dtype_t dtype, int64_t F
                                 int64_t *out_arg, unsigned int *status_word,
                                 seg_stream_t stream);
 
+/*
+ * seg_rle -- run-length encoding of an ordered uint32 vector: the producer
+ * of offsets that groups equal adjacent keys.
+ *
+ * GPURunLengthEncode and GPUUnique (luma.gl API reference), sections "What
+ * is run-length encoding?" and "Contract": every maximal run of adjacent
+ * equal keys becomes one run; runs keep first-occurrence order; equal keys
+ * that are not adjacent start separate runs; an empty input gives zero
+ * runs.  Run r has value values[r], length lengths[r] and starts at
+ * offsets[r]; offsets[count] = n, so offsets delimit the runs as CSR
+ * offsets (lengths [3,2,4] go with offsets [0,3,5,9], the page's "Why RLE
+ * matters for GPU grouping") and can be passed to seg_reduce as they are.
+ * GPUUnique is this call with only `values` requested.
+ *
+ *   keys     device, [n] uint32, aligned to 4 bytes (16 bytes enables
+ *            128-bit loads).  May be NULL only when n == 0.
+ *   n        0 <= n <= UINT32_MAX (lengths are uint32).
+ *   values   device, room for n uint32, aligned to 4 bytes, or NULL.
+ *   lengths  device, room for n uint32, aligned to 4 bytes, or NULL.
+ *   offsets  device, room for n + 1 int64, aligned to 8 bytes, or NULL.
+ *   count    device, one int64, aligned to 8 bytes: receives the number of
+ *            runs.  Required.
+ *   stream   CUDA stream the work is ordered on.
+ *
+ * Only the first count (values, lengths) or count + 1 (offsets) entries are
+ * written.  Inputs and outputs must not overlap.  Scratch is the library's
+ * per-(device, stream) buffer described above.  The call enqueues three
+ * kernel launches and returns without synchronising; the count stays on the
+ * device.  Returns SEG_ERR_INVALID_ARGUMENT for a NULL keys with n > 0, a
+ * NULL count, a negative or too large n, or a misaligned pointer.
+ */
+seg_status_t seg_rle(const uint32_t *keys, int64_t n, uint32_t *values, uint32_t *lengths,
+                     int64_t *offsets, int64_t *count, seg_stream_t stream);
+
+/*
+ * seg_flags_to_offsets -- offsets from segment-start flags.
+ *
+ * GPUSegmentedLayout as GPUSegmentedReduction's "What is an offset-delimited
+ * segment?" names it: it materialises offsets from segment-start flags.
+ * Every index i with flags[i] != 0 starts a segment; the offsets list those
+ * indices in increasing order followed by n.  Rows before the first flag
+ * belong to no segment (the reduction allows offsets[0] > 0).
+ *
+ *   flags    device, [n] bytes (any non-zero byte is a start).  May be NULL
+ *            only when n == 0.  16-byte alignment enables 128-bit loads.
+ *   n        n >= 0.
+ *   offsets  device, room for n + 1 int64, aligned to 8 bytes.  Required.
+ *   count    device, one int64, aligned to 8 bytes: receives the number of
+ *            segments.  Required.
+ *   stream   CUDA stream the work is ordered on.
+ *
+ * Enqueues three kernel launches and returns without synchronising.
+ * Returns SEG_ERR_INVALID_ARGUMENT for a NULL flags with n > 0, a NULL
+ * offsets or count, a negative n, or a misaligned pointer.
+ */
+seg_status_t seg_flags_to_offsets(const uint8_t *flags, int64_t n, int64_t *offsets,
+                                  int64_t *count, seg_stream_t stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t seg_reduce_version(void);
 

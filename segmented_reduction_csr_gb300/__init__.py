@@ -24,6 +24,7 @@ __all__ = [
     "seg_reduce", "segment_sum_csr", "segment_mean_csr", "segment_min_csr",
     "segment_max_csr", "plan", "device_status", "library_path", "load_library",
     "SegReduceError", "seg_reduce_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "seg_rle", "rle", "unique", "seg_flags_to_offsets", "flags_to_offsets",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -37,7 +38,8 @@ STATUS = {0: "SEG_OK", 1: "SEG_ERR_INVALID_ARGUMENT", 2: "SEG_ERR_UNSUPPORTED",
           3: "SEG_ERR_OUT_OF_MEMORY", 4: "SEG_ERR_CUDA", 5: "SEG_ERR_DEVICE_TIMEOUT",
           6: "SEG_ERR_SCRATCH_LIMIT"}
 EXPORTED = ("seg_reduce", "seg_reduce_strerror", "seg_reduce_device_status",
-            "seg_reduce_plan", "seg_reduce_version", "seg_reduce_noalloc")
+            "seg_reduce_plan", "seg_reduce_version", "seg_reduce_noalloc", "seg_rle",
+            "seg_flags_to_offsets")
 NOALLOC_SCRATCH_BYTES = 2 << 20   # SEG_NOALLOC_SCRATCH_BYTES
 
 
@@ -90,6 +92,10 @@ def load_library(path: str | None = None):
         lib.seg_reduce_noalloc.restype = ctypes.c_int
         lib.seg_reduce_noalloc.argtypes = [vp, ctypes.c_int, i64, i64, vp, ctypes.c_int, i64,
                                            ctypes.c_int, vp, vp, vp, vp]
+        lib.seg_rle.restype = ctypes.c_int
+        lib.seg_rle.argtypes = [vp, i64, vp, vp, vp, vp, vp]
+        lib.seg_flags_to_offsets.restype = ctypes.c_int
+        lib.seg_flags_to_offsets.argtypes = [vp, i64, vp, vp, vp]
         if path is None:
             _lib = lib
         return lib
@@ -265,6 +271,103 @@ def segment_max_csr(src, indptr):
 def segment_min_csr(src, indptr):
     """``(values, arg)``: per-segment minimum and its source row."""
     return seg_reduce(src, indptr, "min")
+
+
+def _ptr(t):
+    return t.data_ptr() if t is not None else None
+
+
+def _out_buffer(t, n, dtype, device, name):
+    """A caller's preallocated output (checked) or a new one of n entries."""
+    torch = _torch()
+    if t is None:
+        return torch.empty(n, dtype=dtype, device=device)
+    if t.dtype != dtype or t.dim() != 1 or t.numel() < n or not t.is_contiguous() \
+            or t.device != device:
+        raise ValueError(f"{name} must be a contiguous 1-D {dtype} CUDA tensor of at least {n} entries")
+    return t
+
+
+def seg_rle(keys, values=None, lengths=None, offsets=None, count=None, want_values=True,
+            want_lengths=True, want_offsets=True, stream=None):
+    """Run-length encode ``keys`` ([n] uint32 or int32, CUDA; equality is on
+    the bits) on the device (GPURunLengthEncode / GPUUnique "Contract").
+
+    Returns ``(values, lengths, offsets, count)``: ``values`` (keys' dtype) and
+    ``lengths`` (uint32) hold ``n`` entries and ``offsets`` (int64) ``n + 1``,
+    of which the first ``count`` (``count + 1`` for offsets) are written;
+    ``count`` is a one-element int64 CUDA tensor.  Outputs not wanted are
+    ``None`` and are not written.  Nothing is synchronised; ``rle`` and
+    ``unique`` read the count and trim.
+    """
+    torch = _torch()
+    u32 = getattr(torch, "uint32", None)
+    if not keys.is_cuda:
+        raise ValueError("keys must be a CUDA tensor (there is no CPU path)")
+    if keys.dim() != 1 or not keys.is_contiguous() or keys.dtype not in (torch.int32, u32):
+        raise ValueError("keys must be a contiguous 1-D uint32 or int32 tensor")
+    n = keys.numel()
+    dev = keys.device
+    values = _out_buffer(values, n, keys.dtype, dev, "values") if want_values else None
+    lengths = _out_buffer(lengths, n, u32, dev, "lengths") if want_lengths else None
+    offsets = _out_buffer(offsets, n + 1, torch.int64, dev, "offsets") if want_offsets else None
+    count = _out_buffer(count, 1, torch.int64, dev, "count")
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.seg_rle(keys.data_ptr() if n else None, n, _ptr(values), _ptr(lengths),
+                         _ptr(offsets), count.data_ptr(), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SegReduceError(rc, "seg_rle")
+    return values, lengths, offsets, count
+
+
+def rle(keys):
+    """``(values, lengths, offsets)`` of the runs of ``keys``, trimmed to the
+    run count (reads the count back, so it synchronises)."""
+    values, lengths, offsets, count = seg_rle(keys)
+    c = int(count.item())
+    return values[:c], lengths[:c], offsets[:c + 1]
+
+
+def unique(keys):
+    """The first key of every run of equal adjacent keys (GPUUnique), trimmed
+    to the run count (synchronises)."""
+    values, _, _, count = seg_rle(keys, want_lengths=False, want_offsets=False)
+    return values[:int(count.item())]
+
+
+def seg_flags_to_offsets(flags, offsets=None, count=None, stream=None):
+    """Offsets from segment-start ``flags`` ([n] uint8 or bool, CUDA):
+    every index with a non-zero flag starts a segment; the offsets list those
+    indices, then n (GPUSegmentedLayout).  Returns ``(offsets, count)`` with
+    ``offsets`` of ``n + 1`` int64 entries, the first ``count + 1`` written;
+    not synchronised."""
+    torch = _torch()
+    if not flags.is_cuda:
+        raise ValueError("flags must be a CUDA tensor (there is no CPU path)")
+    if flags.dim() != 1 or not flags.is_contiguous() or flags.dtype not in (torch.uint8, torch.bool):
+        raise ValueError("flags must be a contiguous 1-D uint8 or bool tensor")
+    n = flags.numel()
+    dev = flags.device
+    offsets = _out_buffer(offsets, n + 1, torch.int64, dev, "offsets")
+    count = _out_buffer(count, 1, torch.int64, dev, "count")
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.seg_flags_to_offsets(flags.data_ptr() if n else None, n, offsets.data_ptr(),
+                                      count.data_ptr(), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SegReduceError(rc, "seg_flags_to_offsets")
+    return offsets, count
+
+
+def flags_to_offsets(flags):
+    """``seg_flags_to_offsets`` trimmed to ``count + 1`` entries (synchronises)."""
+    offsets, count = seg_flags_to_offsets(flags)
+    return offsets[:int(count.item()) + 1]
 
 
 def device_status(stream=None) -> int:

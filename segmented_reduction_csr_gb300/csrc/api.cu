@@ -12,6 +12,7 @@
 
 #include "../../include/seg_reduce.h"
 #include "seg_pick.cuh"
+#include "seg_rle.cuh"
 
 using namespace segred;
 
@@ -225,6 +226,38 @@ seg_status_t fixed_state(int dev, cudaStream_t stream, FixedState** out) {
         fs.init = true;
     }
     *out = &fs;
+    return SEG_OK;
+}
+
+// The offsets producers (run-length encoding, flags to offsets): the CTA
+// count, scratch from the (device, stream) buffer past the ticket words
+// (which these launches never touch), then the three launches.
+seg_status_t run_producer(RleParams& p, int64_t n, int64_t* count, cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SEG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* ds = nullptr;
+    seg_status_t st = device_state(dev, &ds);
+    if (st != SEG_OK) return st;
+    p.n = n;
+    p.count = count;
+    p.tiles = ceil_div(n, RLE_TILE);
+    p.ctas = static_cast<int32_t>(std::min<int64_t>(
+        p.tiles, std::min<int64_t>(int64_t(ds->sm_count) * RLE_CTAS_PER_SM, RLE_MAX_CTAS)));
+    const int64_t ticket_bytes = ticket_region_bytes(ds->sm_count);
+    Scratch* sc = nullptr;
+    st = scratch_for(dev, stream, static_cast<size_t>(ticket_bytes + rle_scratch_bytes(RLE_MAX_CTAS)),
+                     &sc);
+    if (st != SEG_OK) return st;
+    int64_t* ws = reinterpret_cast<int64_t*>(static_cast<unsigned char*>(sc->ptr) + ticket_bytes);
+    p.cta_count = ws;
+    p.cta_first = ws + RLE_MAX_CTAS;
+    p.cta_base = ws + 2 * RLE_MAX_CTAS;
+    p.cta_next = ws + 3 * RLE_MAX_CTAS;
+    if (launch_rle(p, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SEG_ERR_CUDA;
+    }
     return SEG_OK;
 }
 
@@ -446,6 +479,34 @@ seg_status_t seg_reduce_noalloc(const void* values, seg_dtype_t dtype, int64_t F
         return SEG_ERR_CUDA;
     }
     return SEG_OK;
+}
+
+seg_status_t seg_rle(const uint32_t* keys, int64_t n, uint32_t* values, uint32_t* lengths,
+                     int64_t* offsets, int64_t* count, seg_stream_t stream) {
+    if (n < 0 || n > int64_t(UINT32_MAX) || !count || (n > 0 && !keys)) return SEG_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(keys) % 4 || reinterpret_cast<uintptr_t>(values) % 4 ||
+        reinterpret_cast<uintptr_t>(lengths) % 4 || reinterpret_cast<uintptr_t>(offsets) % 8 ||
+        reinterpret_cast<uintptr_t>(count) % 8)
+        return SEG_ERR_INVALID_ARGUMENT;
+    RleParams p{};
+    p.keys = keys;
+    p.values = values;
+    p.lengths = lengths;
+    p.offsets = offsets;
+    p.vec = reinterpret_cast<uintptr_t>(keys) % 16 == 0 ? 1 : 0;
+    return run_producer(p, n, count, reinterpret_cast<cudaStream_t>(stream));
+}
+
+seg_status_t seg_flags_to_offsets(const uint8_t* flags, int64_t n, int64_t* offsets,
+                                  int64_t* count, seg_stream_t stream) {
+    if (n < 0 || !count || !offsets || (n > 0 && !flags)) return SEG_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(offsets) % 8 || reinterpret_cast<uintptr_t>(count) % 8)
+        return SEG_ERR_INVALID_ARGUMENT;
+    RleParams p{};
+    p.flags = flags;
+    p.offsets = offsets;
+    p.vec = reinterpret_cast<uintptr_t>(flags) % 16 == 0 ? 1 : 0;
+    return run_producer(p, n, count, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int32_t seg_reduce_version(void) { return kVersion; }

@@ -75,6 +75,26 @@ def test_host_checks_reject_before_any_cuda_call(lib):
     assert _call(lib, op=1, arg=4) == 1                  # misaligned arg
 
 
+def test_producer_host_checks_reject_before_any_cuda_call(lib):
+    # seg_rle(keys, n, values, lengths, offsets, count, stream)
+    assert lib.seg_rle(None, 5, None, None, None, 64, None) == 1          # keys NULL, n > 0
+    assert lib.seg_rle(64, -1, None, None, None, 64, None) == 1           # n < 0
+    assert lib.seg_rle(64, 1 << 32, None, None, None, 64, None) == 1      # n > UINT32_MAX
+    assert lib.seg_rle(64, 5, None, None, None, None, None) == 1          # count NULL
+    assert lib.seg_rle(66, 5, None, None, None, 64, None) == 1            # keys misaligned
+    assert lib.seg_rle(64, 5, 66, None, None, 64, None) == 1              # values misaligned
+    assert lib.seg_rle(64, 5, None, 66, None, 64, None) == 1              # lengths misaligned
+    assert lib.seg_rle(64, 5, None, None, 68, 64, None) == 1              # offsets misaligned
+    assert lib.seg_rle(64, 5, None, None, None, 68, None) == 1            # count misaligned
+    # seg_flags_to_offsets(flags, n, offsets, count, stream)
+    assert lib.seg_flags_to_offsets(None, 5, 64, 64, None) == 1           # flags NULL, n > 0
+    assert lib.seg_flags_to_offsets(64, -2, 64, 64, None) == 1            # n < 0
+    assert lib.seg_flags_to_offsets(64, 5, None, 64, None) == 1           # offsets NULL
+    assert lib.seg_flags_to_offsets(64, 5, 64, None, None) == 1           # count NULL
+    assert lib.seg_flags_to_offsets(65, 5, 68, 64, None) == 1             # offsets misaligned
+    assert lib.seg_flags_to_offsets(65, 5, 64, 60, None) == 1             # count misaligned
+
+
 def test_plan_shapes(lib):
     p = sr.plan("f32", 1, 16_000_000, "i64", 1_000_000, "sum", sm_count=152)
     assert p["grid"] == 152 and p["slot_threads"] == 1 and p["vec"] == 1

@@ -220,3 +220,47 @@ def stats(w: Workload) -> dict:
             "segments": w.num_segments, "empty": int((lengths == 0).sum()),
             "max_len": int(lengths.max()) if lengths.size else 0,
             "over_5M": int((lengths > 5_000_000).sum())}
+
+
+# ---- inputs of the offsets producers (run-length encoding, flags) ----------
+
+def segment_keys(offsets: np.ndarray) -> np.ndarray:
+    """The ordered uint32 key of every row: the id of the segment it falls in
+    (rows before offsets[0] get key 0).  This is the sorted-keys input that
+    run-length encoding turns back into the offsets of the non-empty
+    segments ("sorted keys -> run-length encode -> segment metadata")."""
+    off = offsets.astype(np.int64)
+    keys = np.zeros(int(off[-1]), dtype=np.uint32)
+    lengths = np.diff(off)
+    keys[int(off[0]):] = np.repeat(np.arange(lengths.shape[0], dtype=np.uint32), lengths)
+    return keys
+
+
+def segment_flags(offsets: np.ndarray) -> np.ndarray:
+    """uint8 flags over rows [0, offsets[-1]): 1 where a non-empty segment starts."""
+    off = offsets.astype(np.int64)
+    flags = np.zeros(int(off[-1]), dtype=np.uint8)
+    starts = off[:-1][np.diff(off) > 0]
+    flags[starts] = 1
+    return flags
+
+
+def random_runs(n: int, mean_run: float, seed: int, distinct: int = 1 << 32) -> np.ndarray:
+    """n uint32 keys made of runs with geometric lengths (mean ``mean_run``),
+    each run's key drawn uniformly from [0, distinct).  Neighbouring runs may
+    draw the same key, which merges them (as it should)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if n == 0:
+        return np.zeros(0, dtype=np.uint32)
+    lens = rng.geometric(1.0 / mean_run, size=int(n / mean_run) + 16)
+    while lens.sum() < n:
+        lens = np.concatenate([lens, rng.geometric(1.0 / mean_run, size=lens.shape[0])])
+    keys = rng.integers(0, distinct, size=lens.shape[0], dtype=np.uint64).astype(np.uint32)
+    return np.repeat(keys, lens)[:n]
+
+
+def random_flags(n: int, p: float, seed: int) -> np.ndarray:
+    """n uint8 flags, each non-zero with probability p (non-zero values vary)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    on = rng.random(n) < p
+    return np.where(on, rng.integers(1, 256, size=n), 0).astype(np.uint8)
