@@ -226,10 +226,12 @@ seg_status_t seg_reduce_noalloc(const void *values, seg_dtype_t dtype, int64_t F
  *
  * Only the first count (values, lengths) or count + 1 (offsets) entries are
  * written.  Inputs and outputs must not overlap.  Scratch is the library's
- * per-(device, stream) buffer described above.  The call enqueues three
- * kernel launches and returns without synchronising; the count stays on the
- * device.  Returns SEG_ERR_INVALID_ARGUMENT for a NULL keys with n > 0, a
- * NULL count, a negative or too large n, or a misaligned pointer.
+ * per-(device, stream) buffer described above; these calls grow it to hold
+ * a start bitmap (n / 8 bytes) and 12 bytes per 16,384 elements.  The call
+ * enqueues two kernel launches (one when n == 0) and returns without
+ * synchronising; the count stays on the device.  Returns
+ * SEG_ERR_INVALID_ARGUMENT for a NULL keys with n > 0, a NULL count, a
+ * negative or too large n, or a misaligned pointer.
  */
 seg_status_t seg_rle(const uint32_t *keys, int64_t n, uint32_t *values, uint32_t *lengths,
                      int64_t *offsets, int64_t *count, seg_stream_t stream);
@@ -251,9 +253,11 @@ seg_status_t seg_rle(const uint32_t *keys, int64_t n, uint32_t *values, uint32_t
  *            segments.  Required.
  *   stream   CUDA stream the work is ordered on.
  *
- * Enqueues three kernel launches and returns without synchronising.
- * Returns SEG_ERR_INVALID_ARGUMENT for a NULL flags with n > 0, a NULL
- * offsets or count, a negative n, or a misaligned pointer.
+ * Enqueues two kernel launches (one when n == 0; scratch as for seg_rle)
+ * and returns without synchronising.  Returns SEG_ERR_INVALID_ARGUMENT for a
+ * NULL flags with n > 0, a NULL offsets or count, a negative n, or a
+ * misaligned pointer; SEG_ERR_UNSUPPORTED when n needs more than 2^31 - 1
+ * tiles of 16,384 flags.
  */
 seg_status_t seg_flags_to_offsets(const uint8_t *flags, int64_t n, int64_t *offsets,
                                   int64_t *count, seg_stream_t stream);

@@ -242,18 +242,38 @@ seg_status_t run_producer(RleParams& p, int64_t n, int64_t* count, cudaStream_t 
     p.n = n;
     p.count = count;
     p.tiles = ceil_div(n, RLE_TILE);
+    if (p.tiles > int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;   // one write CTA per tile
     p.ctas = static_cast<int32_t>(std::min<int64_t>(
         p.tiles, std::min<int64_t>(int64_t(ds->sm_count) * RLE_CTAS_PER_SM, RLE_MAX_CTAS)));
+    // scratch past the reduction's ticket words (which these launches never
+    // touch): the per-CTA arrays, then the bitmap
     const int64_t ticket_bytes = ticket_region_bytes(ds->sm_count);
     Scratch* sc = nullptr;
-    st = scratch_for(dev, stream, static_cast<size_t>(ticket_bytes + rle_scratch_bytes(RLE_MAX_CTAS)),
-                     &sc);
+    st = scratch_for(dev, stream,
+                     static_cast<size_t>(ticket_bytes + RLE_CTA_SCRATCH + rle_tile_bytes(p.tiles)), &sc);
     if (st != SEG_OK) return st;
+    // the producers' ticket is slot 0 of the ticket words, tagged with a new
+    // generation like any reduction call on this scratch
+    sc->gen += 1;
+    p.gen = sc->gen;
+    p.ticket = static_cast<unsigned long long*>(sc->ptr);
     int64_t* ws = reinterpret_cast<int64_t*>(static_cast<unsigned char*>(sc->ptr) + ticket_bytes);
     p.cta_count = ws;
     p.cta_first = ws + RLE_MAX_CTAS;
     p.cta_base = ws + 2 * RLE_MAX_CTAS;
     p.cta_next = ws + 3 * RLE_MAX_CTAS;
+    p.tile_first = ws + 4 * RLE_MAX_CTAS;
+    p.tile_count = reinterpret_cast<int32_t*>(p.tile_first + p.tiles);
+    p.bitmap = reinterpret_cast<unsigned long long*>(
+        reinterpret_cast<unsigned char*>(p.tile_first) + ((p.tiles * 12 + 255) / 256) * 256);
+    static const char kProducerKey = 0;
+    if (!ds->configured[&kProducerKey]) {
+        if (configure_rle() != cudaSuccess) {
+            cudaGetLastError();
+            return SEG_ERR_CUDA;
+        }
+        ds->configured[&kProducerKey] = true;
+    }
     if (launch_rle(p, stream) != cudaSuccess) {
         cudaGetLastError();
         return SEG_ERR_CUDA;
@@ -504,6 +524,7 @@ seg_status_t seg_flags_to_offsets(const uint8_t* flags, int64_t n, int64_t* offs
         return SEG_ERR_INVALID_ARGUMENT;
     RleParams p{};
     p.flags = flags;
+    p.flags_mode = 1;
     p.offsets = offsets;
     p.vec = reinterpret_cast<uintptr_t>(flags) % 16 == 0 ? 1 : 0;
     return run_producer(p, n, count, reinterpret_cast<cudaStream_t>(stream));

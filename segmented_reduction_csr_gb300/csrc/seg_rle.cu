@@ -1,6 +1,7 @@
 // seg_rle.cu -- the kernels of the offsets producers (run-length encoding,
 // unique, flags to offsets) and their launcher; the passes are described in
 // seg_rle.cuh.
+#include "seg_common.cuh"
 #include "seg_rle.cuh"
 
 namespace segred {
@@ -9,63 +10,77 @@ namespace {
 constexpr int64_t kNone = INT64_MAX;   // "no start seen"
 constexpr int kWarps = RLE_NT / 32;
 
-// Shared-memory slot of the k-th start of a tile: one pad word per 32
-// entries, so that the all-starts case (thread t writing slots 16t + j)
-// spreads a warp's stores over all 32 banks.
-__device__ __forceinline__ int pad_slot(int k) { return k + (k >> 5); }
-constexpr int kSlots = RLE_TILE + RLE_TILE / 32 + 1;
+// One thread's share of a tile as loaded: RLE_KEYS_PER keys (plus, for lane
+// 0, the key just before them), or RLE_FLAGS_PER flag bytes as 32-bit words.
+template <bool FLAGS>
+struct Raw {
+    static constexpr int PER = FLAGS ? RLE_FLAGS_PER : RLE_KEYS_PER;
+    static constexpr int WORDS = FLAGS ? RLE_FLAGS_PER / 4 : RLE_KEYS_PER;
+    uint32_t w[WORDS];
+    uint32_t before;   // keys: the key before w[0] (lane 0 only; other lanes take it by shuffle)
+};
 
-// My RLE_PER elements starting at `base`: their keys (0 past n) and a bit
-// mask of the ones that start a run (bit j: element base + j).
-__device__ __forceinline__ uint32_t load_starts(const RleParams& p, int64_t base,
-                                                uint32_t (&k)[RLE_PER]) {
-    const int lane = threadIdx.x & 31;
-    uint32_t bits = 0;
-    if (p.keys != nullptr) {
-        if (p.vec && base + RLE_PER <= p.n) {
-            const uint4* q = reinterpret_cast<const uint4*>(p.keys + base);
+template <bool FLAGS>
+__device__ __forceinline__ void load_raw(const RleParams& p, int64_t base, Raw<FLAGS>& r) {
+    constexpr int PER = Raw<FLAGS>::PER;
+    if constexpr (FLAGS) {
+        if (p.vec && base + PER <= p.n) {
+            const uint4* q = reinterpret_cast<const uint4*>(p.flags + base);
 #pragma unroll
-            for (int v = 0; v < RLE_PER / 4; ++v) {
-                const uint4 w = __ldg(q + v);
-                k[4 * v] = w.x;
-                k[4 * v + 1] = w.y;
-                k[4 * v + 2] = w.z;
-                k[4 * v + 3] = w.w;
+            for (int v = 0; v < PER / 16; ++v) {
+                const uint4 x = __ldcs(q + v);
+                r.w[4 * v] = x.x, r.w[4 * v + 1] = x.y, r.w[4 * v + 2] = x.z, r.w[4 * v + 3] = x.w;
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < RLE_PER; ++j) k[j] = base + j < p.n ? __ldg(p.keys + base + j) : 0u;
-        }
-        // the key before my first element: the previous lane's last one, or a load
-        uint32_t before = __shfl_up_sync(0xffffffffu, k[RLE_PER - 1], 1);
-        if (lane == 0) before = base > 0 && base - 1 < p.n ? __ldg(p.keys + base - 1) : 0u;
-#pragma unroll
-        for (int j = 0; j < RLE_PER; ++j) {
-            const uint32_t prev = j == 0 ? before : k[j - 1];
-            const bool start = base + j < p.n && (base + j == 0 || k[j] != prev);
-            bits |= static_cast<uint32_t>(start) << j;
-        }
-    } else {
-        uint32_t w[RLE_PER / 4];
-        if (p.vec && base + RLE_PER <= p.n) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.flags + base));
-            w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
-        } else {
-#pragma unroll
-            for (int q = 0; q < RLE_PER / 4; ++q) {
+            for (int q = 0; q < PER / 4; ++q) {
                 uint32_t x = 0;
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     const int64_t i = base + 4 * q + b;
                     if (i < p.n) x |= static_cast<uint32_t>(__ldg(p.flags + i)) << (8 * b);
                 }
-                w[q] = x;
+                r.w[q] = x;
             }
         }
+        r.before = 0;
+    } else {
+        if (p.vec && base + PER <= p.n) {
+            const uint4* q = reinterpret_cast<const uint4*>(p.keys + base);
 #pragma unroll
-        for (int j = 0; j < RLE_PER; ++j) {
-            k[j] = 0;
-            bits |= static_cast<uint32_t>(((w[j / 4] >> (8 * (j % 4))) & 0xffu) != 0) << j;
+            for (int v = 0; v < PER / 4; ++v) {
+                const uint4 x = __ldcs(q + v);
+                r.w[4 * v] = x.x, r.w[4 * v + 1] = x.y, r.w[4 * v + 2] = x.z, r.w[4 * v + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < PER; ++j) r.w[j] = base + j < p.n ? __ldg(p.keys + base + j) : 0u;
+        }
+        r.before = (threadIdx.x & 31) == 0 && base > 0 && base - 1 < p.n ? __ldg(p.keys + base - 1) : 0u;
+    }
+}
+
+// The mask of my elements that start a run / segment (bit j: element base + j).
+template <bool FLAGS>
+__device__ __forceinline__ unsigned long long start_bits(const RleParams& p, int64_t base,
+                                                         const Raw<FLAGS>& r) {
+    unsigned long long bits = 0;
+    if constexpr (FLAGS) {
+#pragma unroll
+        for (int q = 0; q < RLE_FLAGS_PER / 4; ++q) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                bits |= static_cast<unsigned long long>(((r.w[q] >> (8 * b)) & 0xffu) != 0) << (4 * q + b);
+        }
+    } else {
+        // the key before my first one: the previous lane's last key, or lane 0's load
+        uint32_t before = __shfl_up_sync(0xffffffffu, r.w[RLE_KEYS_PER - 1], 1);
+        if ((threadIdx.x & 31) == 0) before = r.before;
+#pragma unroll
+        for (int j = 0; j < RLE_KEYS_PER; ++j) {
+            const uint32_t prev = j == 0 ? before : r.w[j - 1];
+            const bool start = base + j < p.n && (base + j == 0 || r.w[j] != prev);
+            bits |= static_cast<unsigned long long>(start) << j;
         }
     }
     return bits;
@@ -77,164 +92,258 @@ __device__ __forceinline__ void cta_tiles(const RleParams& p, int64_t& t0, int64
     t1 = p.tiles * (blockIdx.x + 1) / p.ctas;
 }
 
-__global__ void __launch_bounds__(RLE_NT) rle_count_kernel(const RleParams p) {
-    __shared__ int64_t s_cnt[kWarps];
-    __shared__ int64_t s_first[kWarps];
-    int64_t t0, t1;
-    cta_tiles(p, t0, t1);
-    int64_t cnt = 0, first = kNone;
-#pragma unroll 2
-    for (int64_t t = t0; t < t1; ++t) {
-        const int64_t base = t * RLE_TILE + static_cast<int64_t>(threadIdx.x) * RLE_PER;
-        uint32_t k[RLE_PER];
-        const uint32_t bits = load_starts(p, base, k);
-        cnt += __popc(bits);
-        if (bits != 0 && first == kNone) first = base + (__ffs(bits) - 1);
-    }
+// Run by the last count CTA: every CTA's first run index (exclusive sum of
+// the counts) and the first start after its range (suffix minimum of the
+// first starts, capped at n); the run count and offsets[count] = n.  Thread
+// i handles CTAs 4 i .. 4 i + 3.
+__device__ __forceinline__ void scan_ctas(const RleParams& p) {
+    constexpr int PER = RLE_MAX_CTAS / RLE_NT;
+    __shared__ int64_t s_sum[kWarps];
+    __shared__ int64_t s_min[kWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t c[PER], f[PER];
+    int64_t mine = 0, low = kNone;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-        const int64_t f = __shfl_xor_sync(0xffffffffu, first, o);
-        first = f < first ? f : first;
+    for (int k = 0; k < PER; ++k) {
+        const int i = threadIdx.x * PER + k;
+        c[k] = i < p.ctas ? __ldcg(p.cta_count + i) : 0;
+        f[k] = i < p.ctas ? __ldcg(p.cta_first + i) : kNone;
+        mine += c[k];
+        low = f[k] < low ? f[k] : low;
     }
-    if ((threadIdx.x & 31) == 0) {
-        s_cnt[threadIdx.x >> 5] = cnt;
-        s_first[threadIdx.x >> 5] = first;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int64_t c = 0, f = kNone;
-        for (int w = 0; w < kWarps; ++w) {
-            c += s_cnt[w];
-            f = s_first[w] < f ? s_first[w] : f;
-        }
-        p.cta_count[blockIdx.x] = c;
-        p.cta_first[blockIdx.x] = f;
-    }
-}
-
-// One CTA of RLE_MAX_CTAS threads; thread b handles CTA b's entries.
-__global__ void __launch_bounds__(RLE_MAX_CTAS) rle_scan_kernel(const RleParams p) {
-    constexpr int W = RLE_MAX_CTAS / 32;
-    __shared__ int64_t s_sum[W];
-    __shared__ int64_t s_min[RLE_MAX_CTAS + 1];
-    const int b = threadIdx.x, lane = b & 31, warp = b >> 5;
-    const int64_t c = b < p.ctas ? p.cta_count[b] : 0;
-    const int64_t f = b < p.ctas ? p.cta_first[b] : kNone;
-    // exclusive sum of the counts
-    int64_t inc = c;
+    // inclusive prefix sum and inclusive suffix minimum over the warp
+    int64_t inc = mine, suf = low;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int64_t y = __shfl_up_sync(0xffffffffu, inc, o);
         if (lane >= o) inc += y;
+        const int64_t z = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32 && z < suf) suf = z;
     }
     if (lane == 31) s_sum[warp] = inc;
-    s_min[b] = f;
-    if (b == 0) s_min[RLE_MAX_CTAS] = kNone;
+    if (lane == 0) s_min[warp] = suf;
     __syncthreads();
-    int64_t before = 0, total = 0;
-    for (int w = 0; w < W; ++w) {
-        const int64_t x = s_sum[w];
-        before += w < warp ? x : 0;
-        total += x;
+    int64_t before = inc - mine, total = 0, after = kNone;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        before += w < warp ? s_sum[w] : 0;
+        total += s_sum[w];
+        if (w > warp && s_min[w] < after) after = s_min[w];
     }
-    // suffix minimum of the first starts, by doubling
-    for (int o = 1; o < RLE_MAX_CTAS; o <<= 1) {
-        const int64_t y = b + o < RLE_MAX_CTAS ? s_min[b + o] : kNone;
-        __syncthreads();
-        if (y < s_min[b]) s_min[b] = y;
-        __syncthreads();
+    // the minimum over later lanes of my warp
+    int64_t later = __shfl_down_sync(0xffffffffu, suf, 1);
+    if (lane < 31 && later < after) after = later;
+    // my entries, last to first, for the suffix minimum
+#pragma unroll
+    for (int k = PER - 1; k >= 0; --k) {
+        const int i = threadIdx.x * PER + k;
+        int64_t run = before;
+#pragma unroll
+        for (int k2 = 0; k2 < k; ++k2) run += c[k2];
+        if (i < p.ctas) {
+            p.cta_base[i] = run;
+            p.cta_next[i] = after < p.n ? after : p.n;
+        }
+        after = f[k] < after ? f[k] : after;
     }
-    if (b < p.ctas) {
-        const int64_t nx = s_min[b + 1];
-        p.cta_base[b] = before + inc - c;
-        p.cta_next[b] = nx < p.n ? nx : p.n;
-    }
-    if (b == 0) {
+    if (threadIdx.x == 0) {
         *p.count = total;
         if (p.offsets != nullptr) p.offsets[total] = p.n;
     }
 }
 
-__global__ void __launch_bounds__(RLE_NT) rle_write_kernel(const RleParams p) {
-    __shared__ uint32_t s_rel[kSlots];
-    __shared__ uint32_t s_val[kSlots];
-    __shared__ int s_warp[kWarps];
+template <bool FLAGS>
+__global__ void __launch_bounds__(RLE_NT) rle_count_kernel(const RleParams p) {
+    constexpr int PER = Raw<FLAGS>::PER;
+    constexpr int STEP = RLE_NT * PER;        // elements per step
+    constexpr int SPT = RLE_TILE / STEP;      // steps per tile
+    __shared__ int s_cnt[2][kWarps];          // by tile parity: thread 0 reads one while
+    __shared__ int64_t s_first[2][kWarps];    // the warps fill the other
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int64_t t0, t1;
     cta_tiles(p, t0, t1);
-    int64_t run = p.cta_base[blockIdx.x];   // index of the next run to write
-    int64_t pend_r = -1, pend_i = 0;       // thread 0: the run still without a length
-    for (int64_t t = t0; t < t1; ++t) {
-        const int64_t tile0 = t * RLE_TILE;
-        const int64_t base = tile0 + static_cast<int64_t>(threadIdx.x) * RLE_PER;
-        uint32_t k[RLE_PER];
-        const uint32_t bits = load_starts(p, base, k);
-        // block exclusive sum of the start counts
-        const int c = __popc(bits);
-        int inc = c;
+    const int64_t s0 = t0 * SPT, s1 = t1 * SPT;
+    int64_t cta_cnt = 0, cta_first = kNone;   // thread 0: the CTA's totals
+    int tc = 0;                               // my starts in the current tile
+    int64_t tf = kNone;                       // my first start in it
+    const int64_t mine = static_cast<int64_t>(threadIdx.x) * PER;
+    Raw<FLAGS> cur;
+    load_raw<FLAGS>(p, s0 * STEP + mine, cur);
+    for (int64_t st = s0; st < s1; ++st) {
+        Raw<FLAGS> nxt;
+        if (st + 1 < s1) load_raw<FLAGS>(p, (st + 1) * STEP + mine, nxt);
+        const int64_t base = st * STEP + mine;
+        const unsigned long long bits = start_bits<FLAGS>(p, base, cur);
+        // my PER bits of the bitmap (bit i: element i), little-endian within its words
+        if constexpr (FLAGS) p.bitmap[st * RLE_NT + threadIdx.x] = bits;
+        else reinterpret_cast<uint16_t*>(p.bitmap)[st * RLE_NT + threadIdx.x] = static_cast<uint16_t>(bits);
+        tc += __popcll(bits);
+        if (bits != 0 && tf == kNone) tf = base + (__ffsll(static_cast<long long>(bits)) - 1);
+        cur = nxt;
+        if ((st + 1) % SPT == 0) {
+            // the tile is done: its count and first start
+            const int64_t t = st / SPT;
+            const int par = static_cast<int>(t & 1);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += y;
-        }
-        if (lane == 31) s_warp[warp] = inc;
-        __syncthreads();
-        int before = inc - c, total = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const int x = s_warp[w];
-            before += w < warp ? x : 0;
-            total += x;
-        }
-        // my starts, in order, into their slots
-        int slot = before;
-#pragma unroll
-        for (int j = 0; j < RLE_PER; ++j) {
-            if ((bits >> j) & 1u) {
-                s_rel[pad_slot(slot)] = threadIdx.x * RLE_PER + j;
-                s_val[pad_slot(slot)] = k[j];
-                ++slot;
+            for (int o = 16; o > 0; o >>= 1) {
+                tc += __shfl_xor_sync(0xffffffffu, tc, o);
+                const int64_t f = __shfl_xor_sync(0xffffffffu, tf, o);
+                tf = f < tf ? f : tf;
             }
+            if (lane == 0) {
+                s_cnt[par][warp] = tc;
+                s_first[par][warp] = tf;
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int c = 0;
+                int64_t f = kNone;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    c += s_cnt[par][w];
+                    f = s_first[par][w] < f ? s_first[par][w] : f;
+                }
+                p.tile_count[t] = c;
+                p.tile_first[t] = f;
+                cta_cnt += c;
+                cta_first = f < cta_first ? f : cta_first;
+            }
+            tc = 0;
+            tf = kNone;
         }
-        __syncthreads();
-        for (int q = threadIdx.x; q < total; q += RLE_NT) {
-            const int64_t r = run + q;
-            const uint32_t rel = s_rel[pad_slot(q)];
-            if (p.offsets != nullptr) p.offsets[r] = tile0 + rel;
-            if (p.values != nullptr) p.values[r] = s_val[pad_slot(q)];
-            if (p.lengths != nullptr && q + 1 < total) p.lengths[r] = s_rel[pad_slot(q + 1)] - rel;
-        }
-        if (threadIdx.x == 0 && total > 0) {
-            const int64_t first = tile0 + s_rel[pad_slot(0)];
-            if (p.lengths != nullptr && pend_r >= 0)
-                p.lengths[pend_r] = static_cast<uint32_t>(first - pend_i);
-            pend_r = run + total - 1;
-            pend_i = tile0 + s_rel[pad_slot(total - 1)];
-        }
-        run += total;
-        __syncthreads();
     }
-    if (threadIdx.x == 0 && p.lengths != nullptr && pend_r >= 0)
-        p.lengths[pend_r] = static_cast<uint32_t>(p.cta_next[blockIdx.x] - pend_i);
+    __shared__ int s_last;
+    if (threadIdx.x == 0) {
+        p.cta_count[blockIdx.x] = cta_cnt;
+        p.cta_first[blockIdx.x] = cta_first;
+        // the arrival releases the two words above
+        s_last = ticket_last(ticket_take(p.ticket, 0, p.gen), p.gen, p.ctas) ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_last) {
+        fence_acq_rel_gpu();
+        scan_ctas(p);
+    }
+}
+
+// Shared-memory slot of the k-th start of a tile.  Start positions are
+// 16-bit: one pad word per 32 words keeps the all-starts case (thread t
+// writing slots 64 t + j) free of bank conflicts.
+__device__ __forceinline__ int rel_slot(int k) { return k + 2 * (k >> 6); }
+
+// CTA t writes the runs that start in tile t.  Thread i owns bitmap word i:
+// elements tile0 + 64 i + [0, 64).
+__global__ void __launch_bounds__(RLE_NT) rle_write_kernel(const RleParams p) {
+    __shared__ uint16_t s_rel[RLE_TILE + 2 * (RLE_TILE / 64) + 2];
+    __shared__ int s_warp[kWarps];
+    __shared__ int64_t s_run, s_next;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t = blockIdx.x;
+    const int64_t tile0 = t * RLE_TILE;
+    const unsigned long long word = __ldcg(p.bitmap + t * RLE_NT + threadIdx.x);
+    if (warp == 0) {
+        // the count CTA b whose range [t0, t1) holds tile t
+        const int64_t b = ((t + 1) * p.ctas + p.tiles - 1) / p.tiles - 1;
+        const int64_t t0 = p.tiles * b / p.ctas, t1 = p.tiles * (b + 1) / p.ctas;
+        const int64_t b_run = __ldcg(p.cta_base + b), b_after = __ldcg(p.cta_next + b);
+        // runs before the tile: b's base plus the starts of b's tiles before t;
+        // the first start after the tile: in b's later tiles, else after b
+        int64_t runs = 0, nx = kNone;
+        for (int64_t i = t0 + lane; i < t; i += 32) runs += __ldcg(p.tile_count + i);
+        for (int64_t i = t + 1 + lane; i < t1; i += 32) {
+            const int64_t f = __ldcg(p.tile_first + i);
+            nx = f < nx ? f : nx;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            runs += __shfl_xor_sync(0xffffffffu, runs, o);
+            const int64_t f = __shfl_xor_sync(0xffffffffu, nx, o);
+            nx = f < nx ? f : nx;
+        }
+        if (lane == 0) {
+            s_run = b_run + runs;
+            s_next = nx < b_after ? nx : b_after;
+        }
+    }
+    // block exclusive sum of the start counts
+    const int c = __popcll(word);
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) s_warp[warp] = inc;
+    __syncthreads();
+    int slot = inc - c, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const int x = s_warp[w];
+        slot += w < warp ? x : 0;
+        total += x;
+    }
+    // my starts, in order, into their slots
+    unsigned long long b = word;
+    while (b) {
+        const int j = __ffsll(static_cast<long long>(b)) - 1;
+        b &= b - 1;
+        s_rel[rel_slot(slot++)] = static_cast<uint16_t>(threadIdx.x * 64 + j);
+    }
+    __syncthreads();
+    const int64_t run = s_run, next = s_next;
+    const uint32_t* __restrict__ keys = p.keys;
+    uint32_t* __restrict__ values = p.values;
+    uint32_t* __restrict__ lengths = p.lengths;
+    int64_t* __restrict__ offsets = p.offsets;
+#pragma unroll 4
+    for (int q = threadIdx.x; q < total; q += RLE_NT) {
+        const int64_t r = run + q;
+        const int64_t pos = tile0 + s_rel[rel_slot(q)];
+        if (offsets != nullptr) offsets[r] = pos;
+        if (values != nullptr) values[r] = __ldg(keys + pos);
+        if (lengths != nullptr) {
+            const int64_t end = q + 1 < total ? tile0 + s_rel[rel_slot(q + 1)] : next;
+            lengths[r] = static_cast<uint32_t>(end - pos);
+        }
+    }
+}
+
+__global__ void rle_empty_kernel(const RleParams p) {
+    *p.count = 0;
+    if (p.offsets != nullptr) p.offsets[0] = 0;
+}
+
+template <bool FLAGS>
+cudaError_t launch_mode(const RleParams& p, cudaStream_t stream) {
+    if (p.ctas == 0) {
+        rle_empty_kernel<<<1, 1, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
+    rle_count_kernel<FLAGS><<<p.ctas, RLE_NT, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (p.values != nullptr || p.lengths != nullptr || p.offsets != nullptr) {
+        rle_write_kernel<<<static_cast<unsigned>(p.tiles), RLE_NT, 0, stream>>>(p);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+template <class K>
+cudaError_t max_carveout(K kernel) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
 }
 
 }  // namespace
 
+cudaError_t configure_rle() {
+    // all shared memory for the carveout, so that more write CTAs fit per SM
+    return max_carveout(rle_write_kernel);
+}
+
 cudaError_t launch_rle(const RleParams& p, cudaStream_t stream) {
-    if (p.ctas > 0) {
-        rle_count_kernel<<<p.ctas, RLE_NT, 0, stream>>>(p);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    rle_scan_kernel<<<1, RLE_MAX_CTAS, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    if (p.ctas > 0 && (p.values != nullptr || p.lengths != nullptr || p.offsets != nullptr)) {
-        rle_write_kernel<<<p.ctas, RLE_NT, 0, stream>>>(p);
-        e = cudaGetLastError();
-    }
-    return e;
+    return p.flags_mode ? launch_mode<true>(p, stream) : launch_mode<false>(p, stream);
 }
 
 }  // namespace segred

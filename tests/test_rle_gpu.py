@@ -141,6 +141,8 @@ def test_rle_repeated_calls_identical(sr, rle_lib):
         again = [to_host(t) for t in sr.rle(to_dev(keys))]
         for a, b in zip(first, again):
             np.testing.assert_array_equal(a, b)
+    # no tile's look-back ran out of time
+    assert sr.device_status() == 0
 
 
 @pytest.mark.parametrize("name", ["bulk", "skewed"])
