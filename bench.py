@@ -13,6 +13,11 @@ roofline     the reduction kernel against the measured HBM copy bandwidth.
 cpu_baseline the C oracle on the host cores (one thread) over the same cases.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+With --producer rle|unique|flags the step is instead one call of that
+offsets producer over the ordered segment keys (rle, unique) or segment-start
+flags (flags) of the bulk or skewed workload: the input that the producer
+turns back into the workload's offsets.  Its line carries the same keys.
 """
 from __future__ import annotations
 
@@ -385,6 +390,173 @@ def run_ours(args, w: W.Workload):
     return line if rank == 0 else None
 
 
+PRODUCER_METRIC = "offsets-producer effective HBM GB/s (run-length encoding / flags to offsets; 1 GPU)"
+
+
+def producer_input(args, w: W.Workload):
+    if args.producer == "flags":
+        return W.segment_flags(w.offsets)
+    return W.segment_keys(w.offsets)
+
+
+def producer_bytes(args, n: int, runs: int) -> int:
+    """Algorithmic bytes: the input once, the outputs' valid prefixes, the count."""
+    if args.producer == "flags":
+        return n + 8 * (runs + 1) + 8
+    if args.producer == "unique":
+        return 4 * n + 4 * runs + 8
+    return 4 * n + 16 * runs + 8 + 8
+
+
+def producer_config(args, w: W.Workload, n: int, runs: int):
+    what = "segment-start flags (uint8)" if args.producer == "flags" else "ordered segment keys (uint32)"
+    return {"workload": f"{args.producer} over the {what} of the {w.name} workload",
+            "elements": n, "runs": runs, "producer": args.producer,
+            "l2": "flushed before every timed call (2 x L2 write), outside the events"}
+
+
+def run_producer_reference(args, w: W.Workload):
+    import oracle
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    x = producer_input(args, w)
+    f = (lambda: oracle.flags_to_offsets(x)) if args.producer == "flags" else (lambda: oracle.rle(x))
+    r = f()
+    runs = len(r) - 1 if args.producer == "flags" else len(r[0])
+    for _ in range(args.warmup):
+        f()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        f()
+    tot = time.perf_counter() - t0
+    gbs = producer_bytes(args, x.shape[0], runs) * args.steps / tot / 1e9
+    return {"metric": PRODUCER_METRIC, "value": gbs, "unit": "GB/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8" if args.producer == "flags" else "u32",
+            "data": "synthetic", "config": producer_config(args, w, x.shape[0], runs),
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "whole input per step"},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_producer_ours(args, w: W.Workload):
+    import torch
+
+    import segmented_reduction_csr_gb300 as sr
+    from segmented_reduction_csr_gb300 import build as srbuild
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    world, rank = dist_init("nccl", dev)
+    srbuild.build()
+    sr.load_library()
+    x = producer_input(args, w)
+    n = x.shape[0]
+    hx = torch.from_numpy(x.view(np.int32) if x.dtype == np.uint32 else x).pin_memory()
+    dx = hx.to(dev)
+    if x.dtype == np.uint32:
+        dx = dx.view(torch.uint32)
+    stream = torch.cuda.current_stream(dev)
+    flags = args.producer == "flags"
+    if flags:
+        o, c = sr.seg_flags_to_offsets(dx)
+        outs = (None, None, o)
+    else:
+        v, l, o, c = sr.seg_rle(dx, want_lengths=args.producer == "rle", want_offsets=args.producer == "rle")
+        outs = (v, l, o)
+    torch.cuda.synchronize(dev)
+    runs = int(c.item())
+
+    def call():
+        if flags:
+            sr.seg_flags_to_offsets(dx, offsets=outs[2], count=c)
+        else:
+            sr.seg_rle(dx, values=outs[0], lengths=outs[1], offsets=outs[2], count=c,
+                       want_lengths=outs[1] is not None, want_offsets=outs[2] is not None)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    for s, e in ev:
+        flush.zero_()
+        s.record(stream)
+        call()
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    per_call = [s.elapsed_time(e) for s, e in ev]
+    kernel_ms = max_over_ranks(sum(per_call), world, dev)
+    assert sr.device_status(stream) == 0
+    nbytes = producer_bytes(args, n, runs)
+    value = whole_job_gbs(world, nbytes, args.steps, kernel_ms)
+
+    # end to end: the input from pinned host memory, the call, the count and
+    # the valid prefixes of the outputs back to pinned host memory
+    host_outs = [torch.empty(t.numel(), dtype=torch.int32 if t.dtype == torch.uint32 else t.dtype).pin_memory()
+                 if t is not None else None for t in outs]
+    host_c = torch.empty(1, dtype=torch.int64).pin_memory()
+    d2h = 8 + sum((runs + (1 if i == 2 else 0)) * t.element_size() for i, t in enumerate(outs) if t is not None)
+
+    def e2e_step():
+        (dx.view(torch.int32) if dx.dtype == torch.uint32 else dx).copy_(hx, non_blocking=True)
+        call()
+        host_c.copy_(c, non_blocking=True)
+        for i, (t, ht) in enumerate(zip(outs, host_outs)):
+            if t is None:
+                continue
+            k = runs + (1 if i == 2 else 0)
+            ht[:k].copy_((t.view(torch.int32) if t.dtype == torch.uint32 else t)[:k], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = run_producer_reference(argparse.Namespace(steps=1, warmup=0, gpus=1, producer=args.producer), w)["cpu_baseline"]
+    peak, peak_kind = measured_peak()
+    achieved = nbytes * args.steps / (sum(per_call) * 1e-3) / 1e9
+    line = {
+        "metric": PRODUCER_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": kernel_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8" if flags else "u32", "data": "synthetic",
+        "config": producer_config(args, w, n, runs),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "segred::rle_count_kernel + segred::rle_write_kernel (both launches of a call)",
+                     "peak_note": f"{peak_kind} HBM copy bandwidth"},
+        "e2e": {"value": whole_job_gbs(world, nbytes, args.steps, e2e_ms), "unit": "GB/s",
+                "h2d_bytes_per_step": int(hx.numel() * hx.element_size()), "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "us_per_call_median": statistics.median(per_call) * 1e3,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line if rank == 0 else None
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -393,9 +565,18 @@ def main():
     ap.add_argument("--config", default="bulk", choices=W.NAMES)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--producer", default=None, choices=["rle", "unique", "flags"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
+    if args.producer is not None:
+        if args.config not in ("bulk", "skewed"):
+            ap.error("--producer runs on the bulk or skewed workload")
+        w = W.make(args.config, with_values=False)
+        line = run_producer_reference(args, w) if args.impl == "reference" else run_producer_ours(args, w)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
     w = W.make(args.config)
     if args.impl == "reference":
         line = run_reference(args, w)
