@@ -11,6 +11,9 @@ Two independent implementations live here:
   synthetic workloads.
 * ``brute.seg_reduce``: a pure-Python restatement with Python integers and
   ``math.fsum`` for tiny inputs, used to pin the C oracle.
+* ``seg_reduce_sequential``: the input-order float32 sum / mean of
+  ``seq_oracle.c`` (graph-reduce README, "Correctness": the fixed summation
+  order of ``torch.segment_reduce``), pinned by ``brute.seg_reduce_sequential``.
 * ``rle`` / ``flags_to_offsets``: the sequential C loops in ``rle_oracle.c``
   for the producers of offsets (GPURunLengthEncode / GPUUnique,
   GPUSegmentedLayout), pinned by ``brute.rle`` / ``brute.flags_to_offsets``.
@@ -37,6 +40,8 @@ _LIBDIR = os.path.join(_HERE, "lib")
 _LIB = os.path.join(_LIBDIR, "libsegoracle.so")
 _RLE_SRC = os.path.join(_HERE, "rle_oracle.c")
 _RLE_LIB = os.path.join(_LIBDIR, "libsegrleoracle.so")
+_SEQ_SRC = os.path.join(_HERE, "seq_oracle.c")
+_SEQ_LIB = os.path.join(_LIBDIR, "libsegseqoracle.so")
 
 # Codes private to seg_oracle.c.
 _DT = {np.dtype(np.uint32): 0, np.dtype(np.int32): 1, np.dtype(np.float32): 2}
@@ -60,10 +65,10 @@ def compile_source(src: str, dst: str) -> str:
 
 
 def build(force: bool = False) -> str:
-    """Compile seg_oracle.c into lib/libsegoracle.so and rle_oracle.c into
-    lib/libsegrleoracle.so."""
+    """Compile seg_oracle.c into lib/libsegoracle.so, rle_oracle.c into
+    lib/libsegrleoracle.so and seq_oracle.c into lib/libsegseqoracle.so."""
     os.makedirs(_LIBDIR, exist_ok=True)
-    for src, lib in ((_RLE_SRC, _RLE_LIB), (_SRC, _LIB)):
+    for src, lib in ((_RLE_SRC, _RLE_LIB), (_SEQ_SRC, _SEQ_LIB), (_SRC, _LIB)):
         if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(src):
             compile_source(src, lib)
     return _LIB
@@ -175,3 +180,47 @@ def flags_to_offsets(flags, lib=None):
     if count < 0:
         raise ValueError("oracle rejected the input")
     return offsets[: count + 1].copy()
+
+
+_seq_lib = None
+
+
+def load_seq_library(path: str):
+    """ctypes handle of a compiled sequential-sum oracle (the default one, or
+    a deliberately broken copy that a test builds to check the pins)."""
+    lib = ctypes.CDLL(path)
+    lib.oracle_seg_sequential_f32.restype = ctypes.c_int
+    lib.oracle_seg_sequential_f32.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                              ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                              ctypes.c_void_p]
+    return lib
+
+
+def _load_seq():
+    global _seq_lib
+    with _lock:
+        if _seq_lib is None:
+            build()
+            _seq_lib = load_seq_library(_SEQ_LIB)
+    return _seq_lib
+
+
+def seg_reduce_sequential(values, offsets, op: str = "sum", lib=None):
+    """Input-order float32 ``sum`` or ``mean`` of ``values`` ([N] or [N, F]
+    float32) over the segments ``offsets`` ([S+1]) delimits: each sum starts
+    at 0.0f and adds the rows in order, rounding every addition to float32."""
+    if op not in ("sum", "mean"):
+        raise ValueError("the input-order mode is defined for sum and mean")
+    values = np.ascontiguousarray(values, dtype=np.float32)
+    offsets = np.ascontiguousarray(offsets, dtype=np.int64)
+    n = values.shape[0]
+    feat = 1 if values.ndim == 1 else int(np.prod(values.shape[1:]))
+    s = offsets.shape[0] - 1
+    out = np.zeros((s,) + values.shape[1:], dtype=np.float32)
+    lib = _load_seq() if lib is None else lib
+    rc = lib.oracle_seg_sequential_f32(values.ctypes.data if n else None, n, feat,
+                                       offsets.ctypes.data, s, 1 if op == "mean" else 0,
+                                       out.ctypes.data if s else None)
+    if rc != 0:
+        raise ValueError({-1: "bad argument", -2: "offsets not nondecreasing within [0, N]"}.get(rc, rc))
+    return out

@@ -13,6 +13,8 @@ from __future__ import annotations
 import math
 import struct
 
+import numpy as np
+
 
 def _to_f32(x: float) -> float:
     return struct.unpack("<f", struct.pack("<f", x))[0]
@@ -86,3 +88,23 @@ def flags_to_offsets(flags):
     """The indices whose flag is set, then the length (GPUSegmentedLayout)."""
     flags = list(flags)
     return [i for i, f in enumerate(flags) if f] + [len(flags)]
+
+
+def seg_reduce_sequential(values, offsets, op="sum"):
+    """Input-order float32 fold from 0 with numpy float32 scalars, one
+    rounded addition per row (graph-reduce README, "Correctness": fixed
+    summation order); mean divides the float32 sum by the length."""
+    v = np.asarray(values, dtype=np.float32)
+    v2 = v.reshape(v.shape[0], -1)
+    off = [int(x) for x in offsets]
+    out = np.zeros((len(off) - 1, v2.shape[1]), dtype=np.float32)
+    for s in range(len(off) - 1):
+        b, e = off[s], off[s + 1]
+        for f in range(v2.shape[1]):
+            acc = np.float32(0.0)
+            for r in range(b, e):
+                acc = np.float32(acc + v2[r, f])
+            if op == "mean":
+                acc = np.float32(acc / np.float32(e - b)) if e > b else np.float32(0.0)
+            out[s, f] = acc
+    return out.reshape((len(off) - 1,) + v.shape[1:])
