@@ -169,7 +169,12 @@ def whole_job_gbs(world: int, bytes_per_step: int, steps: int, ms: float) -> flo
     return world * bytes_per_step * steps / (ms * 1e-3) / 1e9
 
 
+SEQUENTIAL = False   # --sequential: the input-order float32 sum / mean mode
+
+
 def cases_of(w: W.Workload):
+    if SEQUENTIAL:
+        return [("f32", "sum"), ("f32", "mean")]
     return [(k, op) for k, op in w.cases]
 
 
@@ -187,9 +192,10 @@ def run_reference(args, w: W.Workload):
     cases = cases_of(w)
     offsets = w.offsets
     # bound one step to about 2 s of CPU: prefix of segments
+    reduce = oracle.seg_reduce_sequential if SEQUENTIAL else oracle.seg_reduce
     t0 = time.perf_counter()
     for k, op in cases[:1]:
-        oracle.seg_reduce(w.values[k], offsets, op)
+        reduce(w.values[k], offsets, op)
     one = time.perf_counter() - t0
     est_step = one * len(cases)
     frac = min(1.0, 2.0 / max(est_step, 1e-9))
@@ -201,12 +207,12 @@ def run_reference(args, w: W.Workload):
                        for _, op in cases)
     for _ in range(args.warmup):
         for k, op in cases:
-            oracle.seg_reduce(w.values[k], sub, op)
+            reduce(w.values[k], sub, op)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
         for k, op in cases:
-            oracle.seg_reduce(w.values[k], sub, op)
+            reduce(w.values[k], sub, op)
         times.append(time.perf_counter() - t0)
     tot = sum(times)
     gbs = sample_bytes * args.steps / tot / 1e9
@@ -232,7 +238,8 @@ def config_of(args, w):
         "mp": "1,000,000 rows x 64 float32 into 10,000 segments, int64 indptr",
         "skewed": "64M float32 rows, 1M segments, Zipf(1.5) + 4 giants > 5M, 20% empty",
         "large": "10M rows x 128 float32, 100,000 power-law segments",
-    }[w.name], "segments": w.num_segments, "rows": w.num_rows, "features": w.feat,
+    }[w.name] + ("; input-order float32 mode (seg_reduce_sequential)" if SEQUENTIAL else ""),
+        "segments": w.num_segments, "rows": w.num_rows, "features": w.feat,
         "cases": [f"{k}:{op}" for k, op in cases_of(w)],
         "l2": "flushed before every timed call (2 x L2 write), outside the events"}
 
@@ -272,7 +279,10 @@ def run_ours(args, w: W.Workload):
 
     def call(k, op):
         o, a = outs[(k, op)]
-        sr.seg_reduce(dvals[k], doff, op, out=o, out_arg=a, with_arg=a is not None)
+        if SEQUENTIAL:
+            sr.seg_reduce_sequential(dvals[k], doff, op, out=o)
+        else:
+            sr.seg_reduce(dvals[k], doff, op, out=o, out_arg=a, with_arg=a is not None)
 
     for _ in range(args.warmup):
         for k, op in cases:
@@ -360,20 +370,21 @@ def run_ours(args, w: W.Workload):
 
     peak, peak_kind = measured_peak()
     achieved = bytes_step * args.steps / (sum(per_call) * 1e-3) / 1e9
-    traffic = profile_traffic(w.name)
+    traffic = None if SEQUENTIAL else profile_traffic(w.name)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": kernel_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "u32/s32/f32" if w.feat == 1 else "f32", "data": "synthetic",
+        "dtype": "u32/s32/f32" if (w.feat == 1 and not SEQUENTIAL) else "f32", "data": "synthetic",
         "config": config_of(args, w),
         "pct_of_peak": 100.0 * value / world / peak, "peak_gbs": peak, "peak_kind": peak_kind,
         "pct_of_8tbs": 100.0 * value / world / 8000.0,
         "segments_per_s": world * w.num_segments * len(cases) * args.steps / (kernel_ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": ("segred::seg_scalar_kernel" if w.feat == 1 else "segred::seg_rows2_kernel")
+                     "kernel": ("segred::seg_seq_kernel" if SEQUENTIAL else
+                                ("segred::seg_scalar_kernel" if w.feat == 1 else "segred::seg_rows2_kernel"))
                                + " (every launch of the step)",
                      "peak_note": f"{peak_kind} HBM copy bandwidth"},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -566,7 +577,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--producer", default=None, choices=["rle", "unique", "flags"])
+    ap.add_argument("--sequential", action="store_true",
+                    help="time the input-order float32 sum / mean mode instead")
     args = ap.parse_args()
+    global SEQUENTIAL
+    SEQUENTIAL = args.sequential
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.producer is not None:

@@ -201,6 +201,36 @@ seg_status_t seg_reduce_noalloc(const void *values, seg_dtype_t dtype, int64_t F
                                 seg_stream_t stream);
 
 /*
+ * seg_reduce_sequential -- the input-order float32 mode of the sum and mean.
+ *
+ * graph-reduce README (HF kernels hub), "Correctness": its CSR path is
+ * bitwise equal to torch.segment_reduce because the summation order is
+ * fixed.  Here that order is the input order: out[s, f] starts at 0.0f and
+ * adds values[r, f] for r = offsets[s], ..., offsets[s+1] - 1, each
+ * addition rounded to float32 (round to nearest even); SEG_MEAN divides that
+ * sum by the length as a float32 (one more rounding); an empty segment gives
+ * 0.  The result is a pure function of the inputs, so any machine that adds
+ * in that order reproduces it bit for bit.  seg_reduce's float sums use a
+ * different (also fixed) order and are faster: this call is one chain of
+ * dependent additions per (segment, column), so its time grows with the
+ * longest segment (about one float32 addition latency per row).  min and
+ * max do not depend on the order: use seg_reduce.
+ *
+ *   values, F, num_values, offsets, offsets_dtype, num_segments, out:
+ *            as for seg_reduce, with float32 values and out.
+ *   op       SEG_SUM or SEG_MEAN (SEG_ERR_INVALID_ARGUMENT otherwise).
+ *   stream   CUDA stream the work is ordered on.
+ *
+ * Enqueues one kernel launch (none when num_segments == 0), uses no
+ * scratch, and returns without synchronising.  Argument errors as for
+ * seg_reduce.
+ */
+seg_status_t seg_reduce_sequential(const float *values, int64_t F, int64_t num_values,
+                                   const void *offsets, seg_offset_dtype_t offsets_dtype,
+                                   int64_t num_segments, seg_op_t op, float *out,
+                                   seg_stream_t stream);
+
+/*
  * seg_rle -- run-length encoding of an ordered uint32 vector: the producer
  * of offsets that groups equal adjacent keys.
  *

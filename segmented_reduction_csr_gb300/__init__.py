@@ -25,6 +25,7 @@ __all__ = [
     "segment_max_csr", "plan", "device_status", "library_path", "load_library",
     "SegReduceError", "seg_reduce_noalloc", "NOALLOC_SCRATCH_BYTES",
     "seg_rle", "rle", "unique", "seg_flags_to_offsets", "flags_to_offsets",
+    "seg_reduce_sequential",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -39,7 +40,7 @@ STATUS = {0: "SEG_OK", 1: "SEG_ERR_INVALID_ARGUMENT", 2: "SEG_ERR_UNSUPPORTED",
           6: "SEG_ERR_SCRATCH_LIMIT"}
 EXPORTED = ("seg_reduce", "seg_reduce_strerror", "seg_reduce_device_status",
             "seg_reduce_plan", "seg_reduce_version", "seg_reduce_noalloc", "seg_rle",
-            "seg_flags_to_offsets")
+            "seg_flags_to_offsets", "seg_reduce_sequential")
 NOALLOC_SCRATCH_BYTES = 2 << 20   # SEG_NOALLOC_SCRATCH_BYTES
 
 
@@ -96,6 +97,8 @@ def load_library(path: str | None = None):
         lib.seg_rle.argtypes = [vp, i64, vp, vp, vp, vp, vp]
         lib.seg_flags_to_offsets.restype = ctypes.c_int
         lib.seg_flags_to_offsets.argtypes = [vp, i64, vp, vp, vp]
+        lib.seg_reduce_sequential.restype = ctypes.c_int
+        lib.seg_reduce_sequential.argtypes = [vp, i64, i64, vp, ctypes.c_int, i64, ctypes.c_int, vp, vp]
         if path is None:
             _lib = lib
         return lib
@@ -271,6 +274,47 @@ def segment_max_csr(src, indptr):
 def segment_min_csr(src, indptr):
     """``(values, arg)``: per-segment minimum and its source row."""
     return seg_reduce(src, indptr, "min")
+
+
+def seg_reduce_sequential(values, offsets, op: str = "sum", out=None, stream=None):
+    """The input-order float32 ``sum`` / ``mean`` (graph-reduce README,
+    "Correctness": a fixed summation order): out[s, f] starts at 0.0f and
+    adds the segment's rows in order, rounding each addition to float32;
+    mean divides by the length; empty segments give 0.  ``values`` is
+    float32 ``[N]`` or ``[N, F]`` on CUDA.  Slower than ``seg_reduce`` on long
+    segments (one dependent addition per row); use it for results that must
+    match an in-order float32 loop bit for bit."""
+    torch = _torch()
+    if op not in ("sum", "mean"):
+        raise ValueError("the input-order mode is defined for sum and mean")
+    if not values.is_cuda or not offsets.is_cuda:
+        raise ValueError("values and offsets must be CUDA tensors (there is no CPU path)")
+    if values.dtype != torch.float32:
+        raise TypeError("the input-order mode takes float32 values")
+    if values.device != offsets.device:
+        raise ValueError("values and offsets must be on the same device")
+    if values.dim() not in (1, 2) or offsets.dim() != 1 or offsets.numel() < 1:
+        raise ValueError("values must be [N] or [N, F] and offsets [S+1]")
+    if not values.is_contiguous() or not offsets.is_contiguous():
+        raise ValueError("values and offsets must be contiguous")
+    n = values.shape[0]
+    feat = 1 if values.dim() == 1 else values.shape[1]
+    s = offsets.numel() - 1
+    oshape = (s,) if values.dim() == 1 else (s, feat)
+    if out is None:
+        out = torch.empty(oshape, dtype=torch.float32, device=values.device)
+    elif tuple(out.shape) != oshape or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous float32 tensor of shape {oshape}")
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream(values.device)
+    with torch.cuda.device(values.device):
+        rc = lib.seg_reduce_sequential(values.data_ptr() if n else None, feat, n, offsets.data_ptr(),
+                                       _offset_code(offsets), s, OPS[op], out.data_ptr() if s else None,
+                                       ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SegReduceError(rc, "seg_reduce_sequential")
+    return out
 
 
 def _ptr(t):

@@ -13,6 +13,7 @@
 #include "../../include/seg_reduce.h"
 #include "seg_pick.cuh"
 #include "seg_rle.cuh"
+#include "seg_seq.cuh"
 
 using namespace segred;
 
@@ -528,6 +529,38 @@ seg_status_t seg_flags_to_offsets(const uint8_t* flags, int64_t n, int64_t* offs
     p.offsets = offsets;
     p.vec = reinterpret_cast<uintptr_t>(flags) % 16 == 0 ? 1 : 0;
     return run_producer(p, n, count, reinterpret_cast<cudaStream_t>(stream));
+}
+
+seg_status_t seg_reduce_sequential(const float* values, int64_t F, int64_t num_values,
+                                   const void* offsets, seg_offset_dtype_t offsets_dtype,
+                                   int64_t num_segments, seg_op_t op, float* out,
+                                   seg_stream_t stream) {
+    if (offsets_dtype != SEG_OFF_U32 && offsets_dtype != SEG_OFF_I64) return SEG_ERR_INVALID_ARGUMENT;
+    if (op != SEG_SUM && op != SEG_MEAN) return SEG_ERR_INVALID_ARGUMENT;
+    if (F < 1 || num_values < 0 || num_segments < 0) return SEG_ERR_INVALID_ARGUMENT;
+    if (F > SEG_MAX_FEATURES) return SEG_ERR_UNSUPPORTED;
+    if (num_segments == 0) return SEG_OK;
+    if (!offsets || !out || (num_values > 0 && !values)) return SEG_ERR_INVALID_ARGUMENT;
+    const size_t osz = offsets_dtype == SEG_OFF_U32 ? 4 : 8;
+    if (reinterpret_cast<uintptr_t>(values) % 4 || reinterpret_cast<uintptr_t>(out) % 4 ||
+        reinterpret_cast<uintptr_t>(offsets) % osz)
+        return SEG_ERR_INVALID_ARGUMENT;
+    if (offsets_dtype == SEG_OFF_U32 && num_values > int64_t(UINT32_MAX)) return SEG_ERR_INVALID_ARGUMENT;
+    if (ceil_div(num_segments * F, SEQ_NT) > int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;
+    SeqParams p{};
+    p.values = values;
+    p.offsets = offsets;
+    p.off64 = offsets_dtype == SEG_OFF_I64 ? 1 : 0;
+    p.mean = op == SEG_MEAN ? 1 : 0;
+    p.N = num_values;
+    p.F = F;
+    p.S = num_segments;
+    p.out = out;
+    if (launch_sequential(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SEG_ERR_CUDA;
+    }
+    return SEG_OK;
 }
 
 int32_t seg_reduce_version(void) { return kVersion; }

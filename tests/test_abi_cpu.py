@@ -95,6 +95,24 @@ def test_producer_host_checks_reject_before_any_cuda_call(lib):
     assert lib.seg_flags_to_offsets(65, 5, 64, 60, None) == 1             # count misaligned
 
 
+def test_sequential_host_checks_reject_before_any_cuda_call(lib):
+    # seg_reduce_sequential(values, F, N, offsets, offsets_dtype, S, op, out, stream)
+    seq = lib.seg_reduce_sequential
+    assert seq(64, 1, 10, 64, 1, 0, 0, 64, None) == 0            # S == 0: nothing to do
+    assert seq(64, 1, 10, 64, 1, 3, 1, 64, None) == 1            # min: not an input-order op
+    assert seq(64, 1, 10, 64, 1, 3, 2, 64, None) == 1            # max
+    assert seq(64, 1, 10, 64, 7, 3, 0, 64, None) == 1            # bad offsets dtype
+    assert seq(64, 0, 10, 64, 1, 3, 0, 64, None) == 1            # F < 1
+    assert seq(64, 4096, 10, 64, 1, 3, 0, 64, None) == 2         # F above SEG_MAX_FEATURES
+    assert seq(64, 1, -1, 64, 1, 3, 0, 64, None) == 1            # N < 0
+    assert seq(None, 1, 10, 64, 1, 3, 0, 64, None) == 1          # values NULL with N > 0
+    assert seq(64, 1, 10, None, 1, 3, 0, 64, None) == 1          # offsets NULL
+    assert seq(64, 1, 10, 64, 1, 3, 0, None, None) == 1          # out NULL
+    assert seq(66, 1, 10, 64, 1, 3, 0, 64, None) == 1            # values misaligned
+    assert seq(64, 1, 10, 68, 1, 3, 0, 64, None) == 1            # int64 offsets misaligned
+    assert seq(64, 1, 10, 64, 1, 3, 3, 66, None) == 1            # out misaligned
+
+
 def test_plan_shapes(lib):
     p = sr.plan("f32", 1, 16_000_000, "i64", 1_000_000, "sum", sm_count=152)
     assert p["grid"] == 152 and p["slot_threads"] == 1 and p["vec"] == 1

@@ -102,6 +102,26 @@ def test_brute_force_is_itself_order_sensitive():
     assert math.fsum(float(x) for x in v) == 2.0
 
 
+def test_matches_torch_segment_reduce_on_the_cpu():
+    """graph-reduce README, "Correctness": the fixed-order CSR sum is bitwise
+    equal to torch.segment_reduce.  torch's CPU segment_reduce is an
+    implementation of the same definition written by others: the oracle
+    must agree with it bit for bit, for [N] and [N, F], sum and mean."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(9)
+    for shape, segs in (((4000,), 300), ((3000, 5), 200), ((2000, 64), 50)):
+        v = (rng.standard_normal(shape) * 10.0 ** rng.integers(-3, 8, size=shape)).astype(np.float32)
+        cuts = np.sort(rng.integers(0, shape[0] + 1, size=segs - 1))
+        off = np.concatenate([[0], cuts, [shape[0]]]).astype(np.int64)
+        for op in ("sum", "mean"):
+            exp = torch.segment_reduce(torch.from_numpy(v), op, offsets=torch.from_numpy(off),
+                                       axis=0, unsafe=True).numpy()
+            got = oracle.seg_reduce_sequential(v, off, op)
+            nonempty = np.diff(off) > 0
+            # torch's mean of an empty segment is NaN; the pages' (and this mode's) is 0
+            assert np.array_equal(got[nonempty].view(np.uint32), exp[nonempty].view(np.uint32)), (shape, op)
+
+
 def test_rejects_bad_offsets_and_ops():
     v = np.zeros(4, np.float32)
     with pytest.raises(ValueError):
