@@ -14,6 +14,9 @@ Two independent implementations live here:
 * ``seg_reduce_sequential``: the input-order float32 sum / mean of
   ``seq_oracle.c`` (graph-reduce README, "Correctness": the fixed summation
   order of ``torch.segment_reduce``), pinned by ``brute.seg_reduce_sequential``.
+* ``scatter``: the unsorted scatter of ``scatter_oracle.c`` (graph-reduce
+  README, "API"), pinned against ``seg_reduce`` after a stable sort of the
+  index and against ``brute.scatter``.
 * ``rle`` / ``flags_to_offsets``: the sequential C loops in ``rle_oracle.c``
   for the producers of offsets (GPURunLengthEncode / GPUUnique,
   GPUSegmentedLayout), pinned by ``brute.rle`` / ``brute.flags_to_offsets``.
@@ -40,6 +43,8 @@ _LIBDIR = os.path.join(_HERE, "lib")
 _LIB = os.path.join(_LIBDIR, "libsegoracle.so")
 _RLE_SRC = os.path.join(_HERE, "rle_oracle.c")
 _RLE_LIB = os.path.join(_LIBDIR, "libsegrleoracle.so")
+_SCATTER_SRC = os.path.join(_HERE, "scatter_oracle.c")
+_SCATTER_LIB = os.path.join(_LIBDIR, "libsegscatteroracle.so")
 _SEQ_SRC = os.path.join(_HERE, "seq_oracle.c")
 _SEQ_LIB = os.path.join(_LIBDIR, "libsegseqoracle.so")
 
@@ -66,9 +71,10 @@ def compile_source(src: str, dst: str) -> str:
 
 def build(force: bool = False) -> str:
     """Compile seg_oracle.c into lib/libsegoracle.so, rle_oracle.c into
-    lib/libsegrleoracle.so and seq_oracle.c into lib/libsegseqoracle.so."""
+    lib/libsegrleoracle.so, seq_oracle.c into lib/libsegseqoracle.so and
+    scatter_oracle.c into lib/libsegscatteroracle.so."""
     os.makedirs(_LIBDIR, exist_ok=True)
-    for src, lib in ((_RLE_SRC, _RLE_LIB), (_SEQ_SRC, _SEQ_LIB), (_SRC, _LIB)):
+    for src, lib in ((_RLE_SRC, _RLE_LIB), (_SEQ_SRC, _SEQ_LIB), (_SCATTER_SRC, _SCATTER_LIB), (_SRC, _LIB)):
         if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(src):
             compile_source(src, lib)
     return _LIB
@@ -223,4 +229,55 @@ def seg_reduce_sequential(values, offsets, op: str = "sum", lib=None):
                                        out.ctypes.data if s else None)
     if rc != 0:
         raise ValueError({-1: "bad argument", -2: "offsets not nondecreasing within [0, N]"}.get(rc, rc))
+    return out
+
+
+_scatter_lib = None
+
+
+def load_scatter_library(path: str):
+    """ctypes handle of a compiled scatter oracle (the default one, or a
+    deliberately broken copy that a test builds to check the pins)."""
+    lib = ctypes.CDLL(path)
+    lib.oracle_scatter.restype = ctypes.c_int
+    lib.oracle_scatter.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                   ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                                   ctypes.c_void_p]
+    return lib
+
+
+def _load_scatter():
+    global _scatter_lib
+    with _lock:
+        if _scatter_lib is None:
+            build()
+            _scatter_lib = load_scatter_library(_SCATTER_LIB)
+    return _scatter_lib
+
+
+def scatter(src, index, dim_size: int, op: str, with_arg: bool = True, lib=None):
+    """Scatter the rows of ``src`` ([N] or [N, F]) into ``dim_size`` outputs
+    named by ``index`` ([N] int64): ``sum`` / ``mean`` / ``min`` / ``max``.
+    Returns ``out`` or ``(out, arg)`` for min / max."""
+    src = np.ascontiguousarray(src)
+    if src.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {src.dtype}")
+    index = np.ascontiguousarray(index, dtype=np.int64)
+    n = src.shape[0]
+    feat = 1 if src.ndim == 1 else int(np.prod(src.shape[1:]))
+    if index.shape != (n,):
+        raise ValueError("index must be [N]")
+    shape = (dim_size,) + src.shape[1:]
+    out = np.zeros(shape, dtype=src.dtype)
+    arg = np.full(shape, -1, dtype=np.int64) if op in ("min", "max") else None
+    lib = _load_scatter() if lib is None else lib
+    rc = lib.oracle_scatter(src.ctypes.data if n else None, _DT[src.dtype], feat, n,
+                            index.ctypes.data if n else None, dim_size, _OP[op],
+                            out.ctypes.data if dim_size else None,
+                            arg.ctypes.data if (arg is not None and dim_size) else None)
+    if rc != 0:
+        raise ValueError({-1: "bad argument", -3: "mean is defined for float32 only",
+                          -4: "out of memory"}.get(rc, rc))
+    if arg is not None and with_arg:
+        return out, arg
     return out

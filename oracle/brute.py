@@ -108,3 +108,21 @@ def seg_reduce_sequential(values, offsets, op="sum"):
                 acc = np.float32(acc / np.float32(e - b)) if e > b else np.float32(0.0)
             out[s, f] = acc
     return out.reshape((len(off) - 1,) + v.shape[1:])
+
+
+def scatter(src, index, dim_size, op, kind, feat):
+    """Row-by-row scatter (graph-reduce README, "API"): gather each
+    destination's rows in row order, then reduce them as one segment with
+    ``seg_reduce`` above.  ``src``: list of rows (each a list of F numbers).
+    Returns (out, arg) as lists of rows; an index outside [0, dim_size) is
+    skipped."""
+    groups = [[] for _ in range(dim_size)]
+    for r, d in enumerate(index):
+        if 0 <= int(d) < dim_size:
+            groups[int(d)].append(r)
+    outs, args = [], []
+    for rows in groups:
+        o, a = seg_reduce([src[r] for r in rows], [0, len(rows)], op, kind, feat)
+        outs.append(o[0])
+        args.append([rows[k] if k >= 0 else -1 for k in a[0]])
+    return outs, args
