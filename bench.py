@@ -568,15 +568,167 @@ def run_producer_ours(args, w: W.Workload):
     return line if rank == 0 else None
 
 
+SCATTER_METRIC = "unsorted scatter effective HBM GB/s (graph-reduce scatter_*; 1 GPU)"
+SCATTER_CASES = ("sum", "mean", "max")
+
+
+def scatter_bytes(n: int, feat: int, dim: int, op: str) -> int:
+    """Algorithmic bytes: src and index read once, the outputs (and args) written once."""
+    return n * feat * 4 + n * 8 + dim * feat * 4 + (dim * feat * 8 if op in ("min", "max") else 0)
+
+
+def scatter_config(args, n, feat, dim):
+    return {"workload": f"scatter {args.config}: {n:,} float32 rows x {feat} into {dim:,} outputs, "
+                        "destinations uniform, unsorted (graph-reduce README 'Measured' shape)",
+            "rows": n, "features": feat, "outputs": dim, "cases": [f"f32:{op}" for op in SCATTER_CASES],
+            "l2": "flushed before every timed call (2 x L2 write), outside the events"}
+
+
+def run_scatter_reference(args):
+    import oracle
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    src, idx, dim = W.scatter_input(args.config)
+    n, feat = src.shape
+    for _ in range(args.warmup):
+        oracle.scatter(src, idx, dim, "sum")
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for op in SCATTER_CASES:
+            oracle.scatter(src, idx, dim, op)
+    tot = time.perf_counter() - t0
+    nbytes = sum(scatter_bytes(n, feat, dim, op) for op in SCATTER_CASES)
+    gbs = nbytes * args.steps / tot / 1e9
+    return {"metric": SCATTER_METRIC, "value": gbs, "unit": "GB/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": scatter_config(args, n, feat, dim),
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "whole input, all cases per step"},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_scatter_ours(args):
+    import torch
+
+    import segmented_reduction_csr_gb300 as sr
+    from segmented_reduction_csr_gb300 import build as srbuild
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    world, rank = dist_init("nccl", dev)
+    srbuild.build()
+    sr.load_library()
+    src, idx, dim = W.scatter_input(args.config)
+    n, feat = src.shape
+    hs, hi = torch.from_numpy(src).pin_memory(), torch.from_numpy(idx).pin_memory()
+    ds, di = hs.to(dev), hi.to(dev)
+    outs = {op: (torch.empty((dim, feat), dtype=torch.float32, device=dev),
+                 torch.empty((dim, feat), dtype=torch.int64, device=dev) if op in ("min", "max") else None)
+            for op in SCATTER_CASES}
+    stream = torch.cuda.current_stream(dev)
+
+    def call(op):
+        o, a = outs[op]
+        sr.scatter(ds, di, dim, op, out=o, out_arg=a, with_arg=a is not None)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        for op in SCATTER_CASES:
+            flush.zero_()
+            call(op)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps * len(SCATTER_CASES))]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    k = 0
+    for _ in range(args.steps):
+        for op in SCATTER_CASES:
+            flush.zero_()
+            ev[k][0].record(stream)
+            call(op)
+            ev[k][1].record(stream)
+            k += 1
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    per_call = [s.elapsed_time(e) for s, e in ev]
+    kernel_ms = max_over_ranks(sum(per_call), world, dev)
+    nbytes = sum(scatter_bytes(n, feat, dim, op) for op in SCATTER_CASES)
+    breakdown = []
+    for j, op in enumerate(SCATTER_CASES):
+        ms = statistics.median(per_call[j::len(SCATTER_CASES)])
+        breakdown.append({"case": f"f32:{op}", "us_median": ms * 1e3,
+                          "gbs": scatter_bytes(n, feat, dim, op) / (ms * 1e-3) / 1e9})
+    host_out = {op: (torch.empty((dim, feat), dtype=torch.float32).pin_memory(),
+                     torch.empty((dim, feat), dtype=torch.int64).pin_memory() if outs[op][1] is not None else None)
+                for op in SCATTER_CASES}
+
+    def e2e_step():
+        ds.copy_(hs, non_blocking=True)
+        di.copy_(hi, non_blocking=True)
+        for op in SCATTER_CASES:
+            call(op)
+            host_out[op][0].copy_(outs[op][0], non_blocking=True)
+            if host_out[op][1] is not None:
+                host_out[op][1].copy_(outs[op][1], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    d2h = sum(o.numel() * 4 + (a.numel() * 8 if a is not None else 0) for o, a in host_out.values())
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = run_scatter_reference(argparse.Namespace(steps=1, warmup=0, gpus=1, config=args.config))["cpu_baseline"]
+    peak, peak_kind = measured_peak()
+    achieved = nbytes * args.steps / (sum(per_call) * 1e-3) / 1e9
+    line = {
+        "metric": SCATTER_METRIC, "value": whole_job_gbs(world, nbytes, args.steps, kernel_ms),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": kernel_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": scatter_config(args, n, feat, dim),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "segred::sc_add_kernel / sc_ext_kernel with their fill and finishing launches",
+                     "peak_note": f"{peak_kind} HBM copy bandwidth"},
+        "e2e": {"value": whole_job_gbs(world, nbytes, args.steps, e2e_ms), "unit": "GB/s",
+                "h2d_bytes_per_step": int(hs.numel() * 4 + hi.numel() * 8), "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (2 + 3 + 3),
+        "clocks": clk,
+        "breakdown": breakdown,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line if rank == 0 else None
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="bulk", choices=W.NAMES)
+    ap.add_argument("--config", default="bulk", choices=W.NAMES + ("mp16",))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--producer", default=None, choices=["rle", "unique", "flags"])
+    ap.add_argument("--scatter", action="store_true",
+                    help="time the unsorted scatter path (sum, mean, max) on the mp or mp16 shape")
     ap.add_argument("--sequential", action="store_true",
                     help="time the input-order float32 sum / mean mode instead")
     args = ap.parse_args()
@@ -584,6 +736,13 @@ def main():
     SEQUENTIAL = args.sequential
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
+    if args.scatter:
+        if args.config not in ("mp", "mp16"):
+            ap.error("--scatter runs on the mp or mp16 shape")
+        line = run_scatter_reference(args) if args.impl == "reference" else run_scatter_ours(args)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
     if args.producer is not None:
         if args.config not in ("bulk", "skewed"):
             ap.error("--producer runs on the bulk or skewed workload")

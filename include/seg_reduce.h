@@ -201,6 +201,44 @@ seg_status_t seg_reduce_noalloc(const void *values, seg_dtype_t dtype, int64_t F
                                 seg_stream_t stream);
 
 /*
+ * seg_scatter -- the unsorted scatter path: row r of src goes to output row
+ * index[r].
+ *
+ * graph-reduce README (HF kernels hub), "API": scatter_sum / scatter_add,
+ * scatter_mean (an output that receives no row is 0), scatter_max /
+ * scatter_min returning (values, arg); index is [N] int64.  "Method": one
+ * atomic per element; for max / min the value and its row settle inside one
+ * 64-bit atomic, with ties to the lower row.
+ *
+ *   src        device, [num_rows, F] row-major, element type `dtype`, aligned
+ *              to 4 bytes (16 bytes, with out 16-byte aligned and F % 4 == 0,
+ *              enables 128-bit float32 vector reductions).
+ *   dtype      SEG_U32, SEG_S32 or SEG_F32.
+ *   F          columns, 1 <= F <= SEG_MAX_FEATURES.
+ *   num_rows   N, 0 <= N < 2^32 - 1 (rows are packed into 32 bits).
+ *   index      device, [N] int64, aligned to 8 bytes.  A row whose index is
+ *              outside [0, dim_size) goes nowhere.
+ *   dim_size   D >= 0 output rows; D == 0 returns SEG_OK and launches nothing.
+ *   op         SEG_SUM, SEG_MIN, SEG_MAX, or SEG_MEAN (float32 only).
+ *   out        device, [D, F], element type `dtype`, aligned to 4 bytes.  An
+ *              output that receives no row is 0.
+ *   out_arg    device, [D, F] int64, or NULL: for SEG_MIN / SEG_MAX the row
+ *              holding the extreme (the lowest such row; -1 when none).  It
+ *              must be NULL for SEG_SUM / SEG_MEAN.
+ *
+ * Numerics as for seg_reduce (integer sums wrap modulo 2^32; -0.0 and +0.0
+ * tie), except that float32 sums and means are not reproducible bit for
+ * bit: the order in which the atomics land varies from run to run (the
+ * error stays below 1e-5 * sum(|x|) + 1e-6 per output).  Integer sums and
+ * max / min are deterministic.  Scratch (D * F * 8 bytes for max / min, D * 4
+ * for mean) comes from the library's per-(device, stream) buffer.  Enqueues
+ * two or three kernel launches and returns without synchronising.
+ */
+seg_status_t seg_scatter(const void *src, seg_dtype_t dtype, int64_t F, int64_t num_rows,
+                         const int64_t *index, int64_t dim_size, seg_op_t op, void *out,
+                         int64_t *out_arg, seg_stream_t stream);
+
+/*
  * seg_reduce_sequential -- the input-order float32 mode of the sum and mean.
  *
  * graph-reduce README (HF kernels hub), "Correctness": its CSR path is

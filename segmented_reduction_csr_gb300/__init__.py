@@ -25,7 +25,8 @@ __all__ = [
     "segment_max_csr", "plan", "device_status", "library_path", "load_library",
     "SegReduceError", "seg_reduce_noalloc", "NOALLOC_SCRATCH_BYTES",
     "seg_rle", "rle", "unique", "seg_flags_to_offsets", "flags_to_offsets",
-    "seg_reduce_sequential",
+    "seg_reduce_sequential", "scatter", "scatter_sum", "scatter_add", "scatter_mean",
+    "scatter_max", "scatter_min",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -40,7 +41,7 @@ STATUS = {0: "SEG_OK", 1: "SEG_ERR_INVALID_ARGUMENT", 2: "SEG_ERR_UNSUPPORTED",
           6: "SEG_ERR_SCRATCH_LIMIT"}
 EXPORTED = ("seg_reduce", "seg_reduce_strerror", "seg_reduce_device_status",
             "seg_reduce_plan", "seg_reduce_version", "seg_reduce_noalloc", "seg_rle",
-            "seg_flags_to_offsets", "seg_reduce_sequential")
+            "seg_flags_to_offsets", "seg_reduce_sequential", "seg_scatter")
 NOALLOC_SCRATCH_BYTES = 2 << 20   # SEG_NOALLOC_SCRATCH_BYTES
 
 
@@ -97,6 +98,8 @@ def load_library(path: str | None = None):
         lib.seg_rle.argtypes = [vp, i64, vp, vp, vp, vp, vp]
         lib.seg_flags_to_offsets.restype = ctypes.c_int
         lib.seg_flags_to_offsets.argtypes = [vp, i64, vp, vp, vp]
+        lib.seg_scatter.restype = ctypes.c_int
+        lib.seg_scatter.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp]
         lib.seg_reduce_sequential.restype = ctypes.c_int
         lib.seg_reduce_sequential.argtypes = [vp, i64, i64, vp, ctypes.c_int, i64, ctypes.c_int, vp, vp]
         if path is None:
@@ -274,6 +277,77 @@ def segment_max_csr(src, indptr):
 def segment_min_csr(src, indptr):
     """``(values, arg)``: per-segment minimum and its source row."""
     return seg_reduce(src, indptr, "min")
+
+
+def scatter(src, index, dim_size: int, reduce: str = "sum", out=None, out_arg=None,
+            with_arg: bool = True, stream=None):
+    """Scatter the rows of ``src`` ([N] or [N, F], CUDA) into ``dim_size``
+    outputs named by ``index`` ([N] int64, CUDA) -- graph-reduce README,
+    "API": ``sum`` (or ``add``), ``mean`` (float32; 0 where nothing arrived),
+    ``max`` / ``min`` returning ``(values, arg)`` (the lowest row holding the
+    extreme; 0 and -1 where nothing arrived).  A row whose index is outside
+    [0, dim_size) goes nowhere.  float32 sums and means use atomics and are
+    not bitwise reproducible; use the segmented path (sorted rows and
+    ``seg_reduce``) when they must be.  Not synchronised."""
+    torch = _torch()
+    op = "sum" if reduce == "add" else reduce
+    if op not in OPS:
+        raise ValueError(f"reduce must be one of {sorted(OPS) + ['add']}")
+    if not src.is_cuda or not index.is_cuda:
+        raise ValueError("src and index must be CUDA tensors (there is no CPU path)")
+    if src.device != index.device:
+        raise ValueError("src and index must be on the same device")
+    if src.dim() not in (1, 2) or index.dim() != 1 or index.numel() != src.shape[0]:
+        raise ValueError("src must be [N] or [N, F] and index [N]")
+    if index.dtype != torch.int64:
+        raise TypeError("index must be int64")
+    if not src.is_contiguous() or not index.is_contiguous():
+        raise ValueError("src and index must be contiguous")
+    n = src.shape[0]
+    feat = 1 if src.dim() == 1 else src.shape[1]
+    oshape = (dim_size,) if src.dim() == 1 else (dim_size, feat)
+    if out is None:
+        out = torch.empty(oshape, dtype=src.dtype, device=src.device)
+    elif tuple(out.shape) != oshape or out.dtype != src.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous {src.dtype} tensor of shape {oshape}")
+    want_arg = op in ("min", "max") and (with_arg or out_arg is not None)
+    if want_arg and out_arg is None:
+        out_arg = torch.empty(oshape, dtype=torch.int64, device=src.device)
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream(src.device)
+    with torch.cuda.device(src.device):
+        rc = lib.seg_scatter(src.data_ptr() if n else None, _value_code(src), feat, n,
+                             index.data_ptr() if n else None, dim_size, OPS[op],
+                             out.data_ptr() if dim_size else None,
+                             out_arg.data_ptr() if (want_arg and dim_size) else None,
+                             ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SegReduceError(rc, "seg_scatter")
+    return (out, out_arg) if want_arg else out
+
+
+def scatter_sum(src, index, dim_size):
+    """Sum of the rows sent to each output (graph-reduce README, ``scatter_sum``)."""
+    return scatter(src, index, dim_size, "sum")
+
+
+scatter_add = scatter_sum
+
+
+def scatter_mean(src, index, dim_size):
+    """Mean of the rows sent to each output; 0 where none arrived."""
+    return scatter(src, index, dim_size, "mean")
+
+
+def scatter_max(src, index, dim_size):
+    """``(values, argmax)`` over the rows sent to each output."""
+    return scatter(src, index, dim_size, "max")
+
+
+def scatter_min(src, index, dim_size):
+    """``(values, argmin)`` over the rows sent to each output."""
+    return scatter(src, index, dim_size, "min")
 
 
 def seg_reduce_sequential(values, offsets, op: str = "sum", out=None, stream=None):

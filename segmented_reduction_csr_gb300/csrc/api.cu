@@ -13,6 +13,7 @@
 #include "../../include/seg_reduce.h"
 #include "seg_pick.cuh"
 #include "seg_rle.cuh"
+#include "seg_scatter.cuh"
 #include "seg_seq.cuh"
 
 using namespace segred;
@@ -557,6 +558,60 @@ seg_status_t seg_reduce_sequential(const float* values, int64_t F, int64_t num_v
     p.S = num_segments;
     p.out = out;
     if (launch_sequential(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SEG_ERR_CUDA;
+    }
+    return SEG_OK;
+}
+
+seg_status_t seg_scatter(const void* src, seg_dtype_t dtype, int64_t F, int64_t num_rows,
+                         const int64_t* index, int64_t dim_size, seg_op_t op, void* out,
+                         int64_t* out_arg, seg_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (dtype != SEG_U32 && dtype != SEG_S32 && dtype != SEG_F32) return SEG_ERR_INVALID_ARGUMENT;
+    if (op != SEG_SUM && op != SEG_MIN && op != SEG_MAX && op != SEG_MEAN) return SEG_ERR_INVALID_ARGUMENT;
+    if (F < 1 || num_rows < 0 || dim_size < 0) return SEG_ERR_INVALID_ARGUMENT;
+    if (op == SEG_MEAN && dtype != SEG_F32) return SEG_ERR_UNSUPPORTED;
+    if (F > SEG_MAX_FEATURES) return SEG_ERR_UNSUPPORTED;
+    if ((op == SEG_SUM || op == SEG_MEAN) && out_arg != nullptr) return SEG_ERR_INVALID_ARGUMENT;
+    // rows are packed into 32 bits next to the value for max / min
+    if (num_rows >= int64_t(UINT32_MAX)) return SEG_ERR_UNSUPPORTED;
+    if (dim_size == 0) return SEG_OK;
+    if (!out || (num_rows > 0 && (!src || !index))) return SEG_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(src) % 4 || reinterpret_cast<uintptr_t>(out) % 4 ||
+        reinterpret_cast<uintptr_t>(index) % 8 || reinterpret_cast<uintptr_t>(out_arg) % 8)
+        return SEG_ERR_INVALID_ARGUMENT;
+    if (ceil_div(dim_size * F, 8) > int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SEG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* ds = nullptr;
+    seg_status_t st = device_state(dev, &ds);
+    if (st != SEG_OK) return st;
+    ScatterParams p{};
+    p.src = src;
+    p.index = index;
+    p.N = num_rows;
+    p.F = F;
+    p.D = dim_size;
+    p.dtype = dtype == SEG_F32 ? 2 : (dtype == SEG_S32 ? 1 : 0);
+    p.op = op == SEG_SUM ? 0 : (op == SEG_MIN ? 1 : (op == SEG_MAX ? 2 : 3));
+    p.vec = (dtype == SEG_F32 && F % 4 == 0 && reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
+             reinterpret_cast<uintptr_t>(out) % 16 == 0) ? 4 : 1;
+    p.out = out;
+    p.arg = (op == SEG_MIN || op == SEG_MAX) ? out_arg : nullptr;
+    const int64_t need = (op == SEG_MIN || op == SEG_MAX) ? dim_size * F * 8 : (op == SEG_MEAN ? dim_size * 4 : 0);
+    if (need > 0) {
+        // scratch past the reduction's ticket words, which these launches never touch
+        const int64_t ticket_bytes = ticket_region_bytes(ds->sm_count);
+        Scratch* sc = nullptr;
+        st = scratch_for(dev, stream, static_cast<size_t>(ticket_bytes + need), &sc);
+        if (st != SEG_OK) return st;
+        unsigned char* ws = static_cast<unsigned char*>(sc->ptr) + ticket_bytes;
+        if (op == SEG_MEAN) p.count = reinterpret_cast<uint32_t*>(ws);
+        else p.word = reinterpret_cast<unsigned long long*>(ws);
+    }
+    if (launch_scatter(p, stream) != cudaSuccess) {
         cudaGetLastError();
         return SEG_ERR_CUDA;
     }

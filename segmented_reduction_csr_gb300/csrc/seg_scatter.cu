@@ -1,0 +1,174 @@
+// seg_scatter.cu -- the kernels of the unsorted scatter path (see seg_scatter.cuh).
+#include "seg_scatter.cuh"
+
+namespace segred {
+namespace {
+
+__global__ void __launch_bounds__(SC_NT) sc_fill_kernel(uint32_t* a, int64_t na, uint32_t va,
+                                                        unsigned long long* b, int64_t nb,
+                                                        unsigned long long vb) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * SC_NT;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * SC_NT + threadIdx.x; i < na; i += stride) a[i] = va;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * SC_NT + threadIdx.x; i < nb; i += stride) b[i] = vb;
+}
+
+__device__ __forceinline__ void red_add_v4(float* a, float4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(a), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+
+// sum / mean: item = (row, chunk of VEC columns); SC_ITEMS items per thread,
+// all loads issued before the atomics.
+template <int DT, int VEC>
+__global__ void __launch_bounds__(SC_NT) sc_add_kernel(const ScatterParams p) {
+    const int64_t chunks = p.F / VEC;
+    const int64_t items = p.N * chunks;
+    const int64_t first = (static_cast<int64_t>(blockIdx.x) * SC_NT * SC_ITEMS) + threadIdx.x;
+    int64_t dst[SC_ITEMS], col[SC_ITEMS];
+    float4 fv[SC_ITEMS];
+    uint32_t iv[SC_ITEMS];
+#pragma unroll
+    for (int k = 0; k < SC_ITEMS; ++k) {
+        const int64_t it = first + static_cast<int64_t>(k) * SC_NT;
+        dst[k] = -1;
+        if (it < items) {
+            const int64_t r = it / chunks, c = it - r * chunks;
+            const int64_t d = __ldg(p.index + r);
+            col[k] = c * VEC;
+            if (d >= 0 && d < p.D) {
+                dst[k] = d;
+                if constexpr (DT == 2 && VEC == 4)
+                    fv[k] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.src) + r * p.F) + c);
+                else if constexpr (DT == 2)
+                    fv[k].x = __ldg(static_cast<const float*>(p.src) + r * p.F + c);
+                else
+                    iv[k] = __ldg(static_cast<const uint32_t*>(p.src) + r * p.F + c);
+                if (p.count != nullptr && c == 0) atomicAdd(p.count + d, 1u);
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < SC_ITEMS; ++k) {
+        if (dst[k] < 0) continue;
+        if constexpr (DT == 2 && VEC == 4)
+            red_add_v4(static_cast<float*>(p.out) + dst[k] * p.F + col[k], fv[k]);
+        else if constexpr (DT == 2)
+            atomicAdd(static_cast<float*>(p.out) + dst[k] * p.F + col[k], fv[k].x);
+        else
+            atomicAdd(static_cast<uint32_t*>(p.out) + dst[k] * p.F + col[k], iv[k]);
+    }
+}
+
+// The value's bits in an order-preserving unsigned form (-0.0 as +0.0).
+template <int DT>
+__device__ __forceinline__ uint32_t monotone(uint32_t bits) {
+    if constexpr (DT == 2) {
+        if (bits == 0x80000000u) bits = 0u;
+        return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+    } else if constexpr (DT == 1) {
+        return bits ^ 0x80000000u;
+    } else {
+        return bits;
+    }
+}
+
+// max / min: item = (row, column); the packed word settles value and row.
+template <int DT, bool MAX>
+__global__ void __launch_bounds__(SC_NT) sc_ext_kernel(const ScatterParams p) {
+    const int64_t items = p.N * p.F;
+    const int64_t first = (static_cast<int64_t>(blockIdx.x) * SC_NT * SC_ITEMS) + threadIdx.x;
+    int64_t cell[SC_ITEMS];
+    unsigned long long w[SC_ITEMS];
+#pragma unroll
+    for (int k = 0; k < SC_ITEMS; ++k) {
+        const int64_t it = first + static_cast<int64_t>(k) * SC_NT;
+        cell[k] = -1;
+        if (it < items) {
+            const int64_t r = it / p.F, c = it - r * p.F;
+            const int64_t d = __ldg(p.index + r);
+            if (d >= 0 && d < p.D) {
+                const uint32_t bits = __ldg(static_cast<const uint32_t*>(p.src) + it);
+                const uint32_t lo = MAX ? ~static_cast<uint32_t>(r) : static_cast<uint32_t>(r);
+                w[k] = (static_cast<unsigned long long>(monotone<DT>(bits)) << 32) | lo;
+                cell[k] = d * p.F + c;
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < SC_ITEMS; ++k) {
+        if (cell[k] < 0) continue;
+        if (MAX) atomicMax(p.word + cell[k], w[k]);
+        else atomicMin(p.word + cell[k], w[k]);
+    }
+}
+
+// max / min: the winning row's own value and the row (0 and -1 when none).
+template <bool MAX>
+__global__ void __launch_bounds__(SC_NT) sc_ext_finish_kernel(const ScatterParams p) {
+    const int64_t cells = p.D * p.F;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * SC_NT;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * SC_NT + threadIdx.x; i < cells; i += stride) {
+        const unsigned long long w = p.word[i];
+        const bool none = MAX ? w == 0ull : w == ~0ull;
+        const uint32_t lo = static_cast<uint32_t>(w);
+        const int64_t row = none ? -1 : static_cast<int64_t>(MAX ? ~lo : lo);
+        const int64_t f = i % p.F;
+        static_cast<uint32_t*>(p.out)[i] = none ? 0u : __ldg(static_cast<const uint32_t*>(p.src) + row * p.F + f);
+        if (p.arg != nullptr) p.arg[i] = row;
+    }
+}
+
+__global__ void __launch_bounds__(SC_NT) sc_mean_finish_kernel(const ScatterParams p) {
+    const int64_t cells = p.D * p.F;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * SC_NT;
+    float* out = static_cast<float*>(p.out);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * SC_NT + threadIdx.x; i < cells; i += stride) {
+        const uint32_t n = p.count[i / p.F];
+        out[i] = n > 0 ? __fdiv_rn(out[i], __uint2float_rn(n)) : 0.0f;
+    }
+}
+
+unsigned grid_for(int64_t work, int64_t per_cta) {
+    const int64_t g = (work + per_cta - 1) / per_cta;
+    return static_cast<unsigned>(g < 1 ? 1 : (g > (int64_t(1) << 30) ? (int64_t(1) << 30) : g));
+}
+
+template <int DT>
+cudaError_t launch_dt(const ScatterParams& p, cudaStream_t stream) {
+    const int64_t cells = p.D * p.F;
+    const unsigned gcells = grid_for(cells, SC_NT * 8);
+    const int64_t per = int64_t(SC_NT) * SC_ITEMS;
+    if (p.op == 0 || p.op == 3) {
+        sc_fill_kernel<<<gcells, SC_NT, 0, stream>>>(static_cast<uint32_t*>(p.out), cells, 0u, nullptr, 0, 0ull);
+        if (p.op == 3) sc_fill_kernel<<<grid_for(p.D, SC_NT * 8), SC_NT, 0, stream>>>(p.count, p.D, 0u, nullptr, 0, 0ull);
+        if (p.N > 0) {
+            if (DT == 2 && p.vec == 4)
+                sc_add_kernel<DT, 4><<<grid_for(p.N * (p.F / 4), per), SC_NT, 0, stream>>>(p);
+            else
+                sc_add_kernel<DT, 1><<<grid_for(p.N * p.F, per), SC_NT, 0, stream>>>(p);
+        }
+        if (p.op == 3) sc_mean_finish_kernel<<<gcells, SC_NT, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
+    const bool mx = p.op == 2;
+    sc_fill_kernel<<<gcells, SC_NT, 0, stream>>>(nullptr, 0, 0u, p.word, cells, mx ? 0ull : ~0ull);
+    if (p.N > 0) {
+        const unsigned g = grid_for(p.N * p.F, per);
+        if (mx) sc_ext_kernel<DT, true><<<g, SC_NT, 0, stream>>>(p);
+        else sc_ext_kernel<DT, false><<<g, SC_NT, 0, stream>>>(p);
+    }
+    if (mx) sc_ext_finish_kernel<true><<<gcells, SC_NT, 0, stream>>>(p);
+    else sc_ext_finish_kernel<false><<<gcells, SC_NT, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_scatter(const ScatterParams& p, cudaStream_t stream) {
+    if (p.dtype == 2) return launch_dt<2>(p, stream);
+    if (p.dtype == 1) return launch_dt<1>(p, stream);
+    return launch_dt<0>(p, stream);
+}
+
+}  // namespace segred

@@ -113,6 +113,25 @@ def test_sequential_host_checks_reject_before_any_cuda_call(lib):
     assert seq(64, 1, 10, 64, 1, 3, 3, 66, None) == 1            # out misaligned
 
 
+def test_scatter_host_checks_reject_before_any_cuda_call(lib):
+    # seg_scatter(src, dtype, F, N, index, dim_size, op, out, out_arg, stream)
+    sc = lib.seg_scatter
+    assert sc(64, 2, 1, 10, 64, 0, 0, 64, None, None) == 0          # dim_size 0: nothing to do
+    assert sc(64, 7, 1, 10, 64, 5, 0, 64, None, None) == 1          # bad dtype
+    assert sc(64, 2, 1, 10, 64, 5, 9, 64, None, None) == 1          # bad op
+    assert sc(64, 2, 0, 10, 64, 5, 0, 64, None, None) == 1          # F < 1
+    assert sc(64, 2, 4096, 10, 64, 5, 0, 64, None, None) == 2       # F too large
+    assert sc(64, 0, 1, 10, 64, 5, 3, 64, None, None) == 2          # mean on uint32
+    assert sc(64, 2, 1, 10, 64, 5, 0, 64, 64, None) == 1            # arg with sum
+    assert sc(64, 2, 1, 1 << 32, 64, 5, 2, 64, None, None) == 2     # rows do not fit 32 bits
+    assert sc(None, 2, 1, 10, 64, 5, 0, 64, None, None) == 1        # src NULL
+    assert sc(64, 2, 1, 10, None, 5, 0, 64, None, None) == 1        # index NULL
+    assert sc(64, 2, 1, 10, 64, 5, 0, None, None, None) == 1        # out NULL
+    assert sc(64, 2, 1, 10, 68, 5, 0, 64, None, None) == 1          # index misaligned
+    assert sc(64, 2, 1, 10, 64, 5, 2, 64, 68, None) == 1            # arg misaligned
+    assert sc(64, 2, 1, -1, 64, 5, 0, 64, None, None) == 1          # N < 0
+
+
 def test_plan_shapes(lib):
     p = sr.plan("f32", 1, 16_000_000, "i64", 1_000_000, "sum", sm_count=152)
     assert p["grid"] == 152 and p["slot_threads"] == 1 and p["vec"] == 1

@@ -264,3 +264,19 @@ def random_flags(n: int, p: float, seed: int) -> np.ndarray:
     rng = np.random.Generator(np.random.PCG64(seed))
     on = rng.random(n) < p
     return np.where(on, rng.integers(1, 256, size=n), 0).astype(np.uint8)
+
+
+
+# ---- input of the unsorted scatter path -----------------------------------
+
+def scatter_input(name: str = "mp"):
+    """(src, index, dim_size) for the scatter path: the message-passing shape
+    of the graph-reduce README "Measured" table -- 1,000,000 float32 rows of
+    64 (``mp``) or 16 (``mp16``) columns, N(0, 1), each sent to an output
+    drawn uniformly from 10,000, in no particular order."""
+    feat = {"mp": 64, "mp16": 16}[name]
+    seed = SEED_BASE + 100 + feat
+    rng = np.random.Generator(np.random.PCG64(seed))
+    index = rng.integers(0, 10_000, size=1_000_000).astype(np.int64)
+    src = _fill_values((1_000_000, feat), seed + 1, "normal")
+    return src, index, 10_000
