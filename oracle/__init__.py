@@ -17,6 +17,9 @@ Two independent implementations live here:
 * ``scatter``: the unsorted scatter of ``scatter_oracle.c`` (graph-reduce
   README, "API"), pinned against ``seg_reduce`` after a stable sort of the
   index and against ``brute.scatter``.
+* ``seg_scan``: the segmented inclusive / exclusive scan of
+  ``scan_oracle.c``, pinned against ``seg_reduce`` (every prefix is a
+  reduction), numpy's cumulative routines per segment and ``brute.seg_scan``.
 * ``rle`` / ``flags_to_offsets``: the sequential C loops in ``rle_oracle.c``
   for the producers of offsets (GPURunLengthEncode / GPUUnique,
   GPUSegmentedLayout), pinned by ``brute.rle`` / ``brute.flags_to_offsets``.
@@ -45,6 +48,8 @@ _RLE_SRC = os.path.join(_HERE, "rle_oracle.c")
 _RLE_LIB = os.path.join(_LIBDIR, "libsegrleoracle.so")
 _SCATTER_SRC = os.path.join(_HERE, "scatter_oracle.c")
 _SCATTER_LIB = os.path.join(_LIBDIR, "libsegscatteroracle.so")
+_SCAN_SRC = os.path.join(_HERE, "scan_oracle.c")
+_SCAN_LIB = os.path.join(_LIBDIR, "libsegscanoracle.so")
 _SEQ_SRC = os.path.join(_HERE, "seq_oracle.c")
 _SEQ_LIB = os.path.join(_LIBDIR, "libsegseqoracle.so")
 
@@ -72,9 +77,11 @@ def compile_source(src: str, dst: str) -> str:
 def build(force: bool = False) -> str:
     """Compile seg_oracle.c into lib/libsegoracle.so, rle_oracle.c into
     lib/libsegrleoracle.so, seq_oracle.c into lib/libsegseqoracle.so and
-    scatter_oracle.c into lib/libsegscatteroracle.so."""
+    scatter_oracle.c into lib/libsegscatteroracle.so and scan_oracle.c into
+    lib/libsegscanoracle.so."""
     os.makedirs(_LIBDIR, exist_ok=True)
-    for src, lib in ((_RLE_SRC, _RLE_LIB), (_SEQ_SRC, _SEQ_LIB), (_SCATTER_SRC, _SCATTER_LIB), (_SRC, _LIB)):
+    for src, lib in ((_RLE_SRC, _RLE_LIB), (_SEQ_SRC, _SEQ_LIB), (_SCATTER_SRC, _SCATTER_LIB),
+                     (_SCAN_SRC, _SCAN_LIB), (_SRC, _LIB)):
         if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(src):
             compile_source(src, lib)
     return _LIB
@@ -280,4 +287,44 @@ def scatter(src, index, dim_size: int, op: str, with_arg: bool = True, lib=None)
                           -4: "out of memory"}.get(rc, rc))
     if arg is not None and with_arg:
         return out, arg
+    return out
+
+
+_scan_lib = None
+
+
+def load_scan_library(path: str):
+    """ctypes handle of a compiled scan oracle (the default one, or a
+    deliberately broken copy that a test builds to check the pins)."""
+    lib = ctypes.CDLL(path)
+    lib.oracle_seg_scan.restype = ctypes.c_int
+    lib.oracle_seg_scan.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
+                                    ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    return lib
+
+
+def _load_scan():
+    global _scan_lib
+    with _lock:
+        if _scan_lib is None:
+            build()
+            _scan_lib = load_scan_library(_SCAN_LIB)
+    return _scan_lib
+
+
+def seg_scan(values, offsets, op: str = "sum", exclusive: bool = False, lib=None):
+    """Segmented scan of ``values`` ([N], uint32 / int32 / float32) over the
+    segments ``offsets`` ([S+1]) delimits; rows in no segment give 0."""
+    values = np.ascontiguousarray(values)
+    if values.dtype not in _DT or values.ndim != 1:
+        raise TypeError("values must be a 1-D uint32, int32 or float32 array")
+    offsets = np.ascontiguousarray(offsets, dtype=np.int64)
+    n = values.shape[0]
+    out = np.empty(n, dtype=values.dtype)
+    lib = _load_scan() if lib is None else lib
+    rc = lib.oracle_seg_scan(values.ctypes.data if n else None, _DT[values.dtype], n,
+                             offsets.ctypes.data, offsets.shape[0] - 1, _OP[op], 1 if exclusive else 0,
+                             out.ctypes.data if n else None)
+    if rc != 0:
+        raise ValueError({-1: "bad argument", -2: "offsets not nondecreasing within [0, N]"}.get(rc, rc))
     return out

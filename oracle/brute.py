@@ -126,3 +126,20 @@ def scatter(src, index, dim_size, op, kind, feat):
         outs.append(o[0])
         args.append([rows[k] if k >= 0 else -1 for k in a[0]])
     return outs, args
+
+
+def seg_scan(values, offsets, op, kind, exclusive=False):
+    """Every prefix of every segment reduced by ``seg_reduce`` above (one
+    segment per prefix): out[r] for offsets[s] <= r < offsets[s+1] is the
+    reduction of values[offsets[s] .. r] (.. r - 1 when exclusive, sum only);
+    rows in no segment are 0."""
+    values = list(values)
+    out = [0.0 if kind == "f32" else 0] * len(values)
+    off = [int(x) for x in offsets]
+    for s in range(len(off) - 1):
+        for r in range(off[s], off[s + 1]):
+            end = r if exclusive else r + 1
+            rows = [[values[i]] for i in range(off[s], end)]
+            o, _ = seg_reduce(rows, [0, len(rows)], op, kind, 1)
+            out[r] = o[0][0]
+    return out
