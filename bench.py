@@ -170,16 +170,28 @@ def whole_job_gbs(world: int, bytes_per_step: int, steps: int, ms: float) -> flo
 
 
 SEQUENTIAL = False   # --sequential: the input-order float32 sum / mean mode
+SCAN = False         # --scan: the segmented scan (inclusive sum and max)
 
 
 def cases_of(w: W.Workload):
     if SEQUENTIAL:
         return [("f32", "sum"), ("f32", "mean")]
+    if SCAN:
+        return [("f32", "sum"), ("f32", "max")]
     return [(k, op) for k, op in w.cases]
 
 
+def case_bytes(w: W.Workload, kind: str, op: str) -> int:
+    """Algorithmic bytes of one call: a scan reads the values and offsets and
+    writes one value per row; a reduction is counted by workloads.workload_bytes."""
+    if SCAN:
+        n = int(next(iter(w.values.values())).shape[0])
+        return 8 * n + w.offsets.nbytes
+    return W.workload_bytes(w, kind, op)
+
+
 def step_bytes(w: W.Workload) -> int:
-    return sum(W.workload_bytes(w, k, op) for k, op in cases_of(w))
+    return sum(case_bytes(w, k, op) for k, op in cases_of(w))
 
 
 def run_reference(args, w: W.Workload):
@@ -192,7 +204,12 @@ def run_reference(args, w: W.Workload):
     cases = cases_of(w)
     offsets = w.offsets
     # bound one step to about 2 s of CPU: prefix of segments
-    reduce = oracle.seg_reduce_sequential if SEQUENTIAL else oracle.seg_reduce
+    if SCAN:
+        def reduce(v, off, op):
+            # the scan of the rows the prefix of offsets covers
+            return oracle.seg_scan(v[: int(off[-1])], off, op)
+    else:
+        reduce = oracle.seg_reduce_sequential if SEQUENTIAL else oracle.seg_reduce
     t0 = time.perf_counter()
     for k, op in cases[:1]:
         reduce(w.values[k], offsets, op)
@@ -203,7 +220,8 @@ def run_reference(args, w: W.Workload):
     s_take = max(1, int(S * frac))
     sub = offsets[: s_take + 1]
     rows = int(sub[-1]) - int(sub[0])
-    sample_bytes = sum(W.algorithmic_bytes(rows, w.feat, s_take, offsets.dtype.itemsize, op)
+    sample_bytes = sum((8 * int(sub[-1]) + sub.nbytes) if SCAN else
+                       W.algorithmic_bytes(rows, w.feat, s_take, offsets.dtype.itemsize, op)
                        for _, op in cases)
     for _ in range(args.warmup):
         for k, op in cases:
@@ -238,7 +256,8 @@ def config_of(args, w):
         "mp": "1,000,000 rows x 64 float32 into 10,000 segments, int64 indptr",
         "skewed": "64M float32 rows, 1M segments, Zipf(1.5) + 4 giants > 5M, 20% empty",
         "large": "10M rows x 128 float32, 100,000 power-law segments",
-    }[w.name] + ("; input-order float32 mode (seg_reduce_sequential)" if SEQUENTIAL else ""),
+    }[w.name] + ("; input-order float32 mode (seg_reduce_sequential)" if SEQUENTIAL else "")
+      + ("; segmented scan (seg_scan), inclusive" if SCAN else ""),
         "segments": w.num_segments, "rows": w.num_rows, "features": w.feat,
         "cases": [f"{k}:{op}" for k, op in cases_of(w)],
         "l2": "flushed before every timed call (2 x L2 write), outside the events"}
@@ -270,8 +289,10 @@ def run_ours(args, w: W.Workload):
     outs = {}
     for k, op in cases:
         shape = (w.num_segments,) if w.feat == 1 else (w.num_segments, w.feat)
+        if SCAN:
+            shape = (w.num_rows,)
         o = torch.empty(shape, dtype=dvals[k].dtype, device=dev)
-        a = torch.empty(shape, dtype=torch.int64, device=dev) if op in ("min", "max") else None
+        a = torch.empty(shape, dtype=torch.int64, device=dev) if (op in ("min", "max") and not SCAN) else None
         outs[(k, op)] = (o, a)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
@@ -279,7 +300,9 @@ def run_ours(args, w: W.Workload):
 
     def call(k, op):
         o, a = outs[(k, op)]
-        if SEQUENTIAL:
+        if SCAN:
+            sr.seg_scan(dvals[k], doff, op, out=o)
+        elif SEQUENTIAL:
             sr.seg_reduce_sequential(dvals[k], doff, op, out=o)
         else:
             sr.seg_reduce(dvals[k], doff, op, out=o, out_arg=a, with_arg=a is not None)
@@ -322,7 +345,7 @@ def run_ours(args, w: W.Workload):
     breakdown = []
     for k, op in cases:
         ms = statistics.median(by_case[(k, op)])
-        b = W.workload_bytes(w, k, op)
+        b = case_bytes(w, k, op)
         breakdown.append({"case": f"{k}:{op}", "us_median": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
                           "bytes": b})
 
@@ -370,7 +393,7 @@ def run_ours(args, w: W.Workload):
 
     peak, peak_kind = measured_peak()
     achieved = bytes_step * args.steps / (sum(per_call) * 1e-3) / 1e9
-    traffic = None if SEQUENTIAL else profile_traffic(w.name)
+    traffic = None if (SEQUENTIAL or SCAN) else profile_traffic(w.name)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -383,7 +406,8 @@ def run_ours(args, w: W.Workload):
         "segments_per_s": world * w.num_segments * len(cases) * args.steps / (kernel_ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": ("segred::seg_seq_kernel" if SEQUENTIAL else
+                     "kernel": ("segred::rs_scan_kernel + rs_fix_kernel (with the bitmap launches)" if SCAN else
+                                "segred::seg_seq_kernel" if SEQUENTIAL else
                                 ("segred::seg_scalar_kernel" if w.feat == 1 else "segred::seg_rows2_kernel"))
                                + " (every launch of the step)",
                      "peak_note": f"{peak_kind} HBM copy bandwidth"},
@@ -729,11 +753,14 @@ def main():
     ap.add_argument("--producer", default=None, choices=["rle", "unique", "flags"])
     ap.add_argument("--scatter", action="store_true",
                     help="time the unsorted scatter path (sum, mean, max) on the mp or mp16 shape")
+    ap.add_argument("--scan", action="store_true",
+                    help="time the segmented scan (inclusive float32 sum and max) instead")
     ap.add_argument("--sequential", action="store_true",
                     help="time the input-order float32 sum / mean mode instead")
     args = ap.parse_args()
-    global SEQUENTIAL
+    global SEQUENTIAL, SCAN
     SEQUENTIAL = args.sequential
+    SCAN = args.scan
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.scatter:

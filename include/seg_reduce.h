@@ -201,6 +201,41 @@ seg_status_t seg_reduce_noalloc(const void *values, seg_dtype_t dtype, int64_t F
                                 seg_stream_t stream);
 
 /*
+ * seg_scan -- segmented scan over the same offsets.
+ *
+ * The pages name a segmented scan (GPUSegmentedScan, beside GPUScan on the
+ * luma.gl GPURunLengthEncode page) without defining it; the segments are
+ * GPUSegmentedReduction's ("What is an offset-delimited segment?").  For
+ * every row r of segment s (offsets[s] <= r < offsets[s+1]):
+ *   inclusive: out[r] = op(values[offsets[s]], ..., values[r]);
+ *   exclusive (SEG_SUM only): out[r] = sum(values[offsets[s] .. r - 1]),
+ *     0 at the segment's first row;
+ * and out[r] = 0 for a row in no segment (before offsets[0] or from
+ * offsets[S] on).  Integer sums wrap modulo 2^32; uint32 compares unsigned,
+ * sint32 signed, float32 by IEEE '<' / '>'.  float32 sums are not in row
+ * order; the order is a pure function of (num_values, offsets, the SM count)
+ * and the error stays below 1e-5 * sum(|x| over the row's prefix) + 1e-6.
+ *
+ *   values         device, [num_values] of `dtype`, aligned to 4 bytes (16
+ *                  bytes, with out 16-byte aligned, enables 128-bit loads).
+ *   num_values     N >= 0; N == 0 returns SEG_OK and launches nothing.
+ *   offsets, offsets_dtype, num_segments: as for seg_reduce (S >= 0; with
+ *                  S == 0 every row is in no segment).
+ *   op             SEG_SUM, SEG_MIN or SEG_MAX.
+ *   exclusive      0 or 1 (1 only with SEG_SUM, else SEG_ERR_UNSUPPORTED).
+ *   out            device, [num_values] of `dtype`, aligned to 4 bytes; must
+ *                  not overlap values.
+ *
+ * Scratch (a start bitmap of N / 8 bytes and 36 KiB of per-CTA words) comes
+ * from the library's per-(device, stream) buffer.  Enqueues four kernel
+ * launches and returns without synchronising.
+ */
+seg_status_t seg_scan(const void *values, seg_dtype_t dtype, int64_t num_values,
+                      const void *offsets, seg_offset_dtype_t offsets_dtype,
+                      int64_t num_segments, seg_op_t op, int32_t exclusive, void *out,
+                      seg_stream_t stream);
+
+/*
  * seg_scatter -- the unsorted scatter path: row r of src goes to output row
  * index[r].
  *

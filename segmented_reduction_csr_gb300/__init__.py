@@ -26,7 +26,7 @@ __all__ = [
     "SegReduceError", "seg_reduce_noalloc", "NOALLOC_SCRATCH_BYTES",
     "seg_rle", "rle", "unique", "seg_flags_to_offsets", "flags_to_offsets",
     "seg_reduce_sequential", "scatter", "scatter_sum", "scatter_add", "scatter_mean",
-    "scatter_max", "scatter_min",
+    "scatter_max", "scatter_min", "seg_scan", "segment_cumsum_csr",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -41,7 +41,7 @@ STATUS = {0: "SEG_OK", 1: "SEG_ERR_INVALID_ARGUMENT", 2: "SEG_ERR_UNSUPPORTED",
           6: "SEG_ERR_SCRATCH_LIMIT"}
 EXPORTED = ("seg_reduce", "seg_reduce_strerror", "seg_reduce_device_status",
             "seg_reduce_plan", "seg_reduce_version", "seg_reduce_noalloc", "seg_rle",
-            "seg_flags_to_offsets", "seg_reduce_sequential", "seg_scatter")
+            "seg_flags_to_offsets", "seg_reduce_sequential", "seg_scatter", "seg_scan")
 NOALLOC_SCRATCH_BYTES = 2 << 20   # SEG_NOALLOC_SCRATCH_BYTES
 
 
@@ -98,6 +98,8 @@ def load_library(path: str | None = None):
         lib.seg_rle.argtypes = [vp, i64, vp, vp, vp, vp, vp]
         lib.seg_flags_to_offsets.restype = ctypes.c_int
         lib.seg_flags_to_offsets.argtypes = [vp, i64, vp, vp, vp]
+        lib.seg_scan.restype = ctypes.c_int
+        lib.seg_scan.argtypes = [vp, ctypes.c_int, i64, vp, ctypes.c_int, i64, ctypes.c_int, i32, vp, vp]
         lib.seg_scatter.restype = ctypes.c_int
         lib.seg_scatter.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp]
         lib.seg_reduce_sequential.restype = ctypes.c_int
@@ -277,6 +279,47 @@ def segment_max_csr(src, indptr):
 def segment_min_csr(src, indptr):
     """``(values, arg)``: per-segment minimum and its source row."""
     return seg_reduce(src, indptr, "min")
+
+
+def seg_scan(values, offsets, op: str = "sum", exclusive: bool = False, out=None, stream=None):
+    """Segmented scan of ``values`` ([N], uint32 / int32 / float32, CUDA) over
+    the segments ``offsets`` ([S+1], int64 or uint32, CUDA) delimits: for a
+    row of segment s, the inclusive ``sum`` / ``min`` / ``max`` of the
+    segment's rows up to it, or (``exclusive``, sum only) of the rows before
+    it; rows in no segment give 0.  Not synchronised."""
+    torch = _torch()
+    if op not in ("sum", "min", "max"):
+        raise ValueError("op must be sum, min or max")
+    if exclusive and op != "sum":
+        raise ValueError("the exclusive scan is defined for sum")
+    if not values.is_cuda or not offsets.is_cuda:
+        raise ValueError("values and offsets must be CUDA tensors (there is no CPU path)")
+    if values.device != offsets.device:
+        raise ValueError("values and offsets must be on the same device")
+    if values.dim() != 1 or offsets.dim() != 1 or offsets.numel() < 1:
+        raise ValueError("values must be [N] and offsets [S+1]")
+    if not values.is_contiguous() or not offsets.is_contiguous():
+        raise ValueError("values and offsets must be contiguous")
+    n = values.numel()
+    if out is None:
+        out = torch.empty_like(values)
+    elif out.shape != values.shape or out.dtype != values.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like values")
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream(values.device)
+    with torch.cuda.device(values.device):
+        rc = lib.seg_scan(values.data_ptr() if n else None, _value_code(values), n, offsets.data_ptr(),
+                          _offset_code(offsets), offsets.numel() - 1, OPS[op], 1 if exclusive else 0,
+                          out.data_ptr() if n else None, ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SegReduceError(rc, "seg_scan")
+    return out
+
+
+def segment_cumsum_csr(src, indptr):
+    """Inclusive per-segment cumulative sum (``seg_scan`` with ``sum``)."""
+    return seg_scan(src, indptr, "sum")
 
 
 def scatter(src, index, dim_size: int, reduce: str = "sum", out=None, out_arg=None,

@@ -13,6 +13,7 @@
 #include "../../include/seg_reduce.h"
 #include "seg_pick.cuh"
 #include "seg_rle.cuh"
+#include "seg_scan.cuh"
 #include "seg_scatter.cuh"
 #include "seg_seq.cuh"
 
@@ -612,6 +613,70 @@ seg_status_t seg_scatter(const void* src, seg_dtype_t dtype, int64_t F, int64_t 
         else p.word = reinterpret_cast<unsigned long long*>(ws);
     }
     if (launch_scatter(p, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SEG_ERR_CUDA;
+    }
+    return SEG_OK;
+}
+
+seg_status_t seg_scan(const void* values, seg_dtype_t dtype, int64_t num_values, const void* offsets,
+                      seg_offset_dtype_t offsets_dtype, int64_t num_segments, seg_op_t op,
+                      int32_t exclusive, void* out, seg_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (dtype != SEG_U32 && dtype != SEG_S32 && dtype != SEG_F32) return SEG_ERR_INVALID_ARGUMENT;
+    if (offsets_dtype != SEG_OFF_U32 && offsets_dtype != SEG_OFF_I64) return SEG_ERR_INVALID_ARGUMENT;
+    if (op != SEG_SUM && op != SEG_MIN && op != SEG_MAX) return SEG_ERR_INVALID_ARGUMENT;
+    if (exclusive != 0 && exclusive != 1) return SEG_ERR_INVALID_ARGUMENT;
+    if (exclusive && op != SEG_SUM) return SEG_ERR_UNSUPPORTED;
+    if (num_values < 0 || num_segments < 0) return SEG_ERR_INVALID_ARGUMENT;
+    if (num_values == 0) return SEG_OK;
+    if (!values || !offsets || !out) return SEG_ERR_INVALID_ARGUMENT;
+    const size_t osz = offsets_dtype == SEG_OFF_U32 ? 4 : 8;
+    if (reinterpret_cast<uintptr_t>(values) % 4 || reinterpret_cast<uintptr_t>(out) % 4 ||
+        reinterpret_cast<uintptr_t>(offsets) % osz)
+        return SEG_ERR_INVALID_ARGUMENT;
+    if (offsets_dtype == SEG_OFF_U32 && num_values > int64_t(UINT32_MAX)) return SEG_ERR_INVALID_ARGUMENT;
+    const int64_t tiles = ceil_div(num_values, RS_TILE);
+    if (tiles > int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SEG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* ds = nullptr;
+    seg_status_t st = device_state(dev, &ds);
+    if (st != SEG_OK) return st;
+    // scratch past the reduction's ticket words: per-CTA words, then the bitmap;
+    // the ticket is slot 0 of the ticket words, tagged with a new generation
+    const int64_t ticket_bytes = ticket_region_bytes(ds->sm_count);
+    const int64_t cta_bytes = int64_t(RS_MAX_CTAS) * (8 + 8 + 8 + 4 + 4 + 4);
+    const int64_t bitmap_bytes = rs_bitmap_words(num_values) * 8;
+    Scratch* sc = nullptr;
+    st = scratch_for(dev, stream, static_cast<size_t>(ticket_bytes + cta_bytes + bitmap_bytes), &sc);
+    if (st != SEG_OK) return st;
+    sc->gen += 1;
+    unsigned char* ws = static_cast<unsigned char*>(sc->ptr) + ticket_bytes;
+    ScanParams p{};
+    p.values = values;
+    p.offsets = offsets;
+    p.off64 = offsets_dtype == SEG_OFF_I64 ? 1 : 0;
+    p.dtype = dtype == SEG_F32 ? 2 : (dtype == SEG_S32 ? 1 : 0);
+    p.op = op == SEG_SUM ? 0 : (op == SEG_MIN ? 1 : 2);
+    p.exclusive = exclusive;
+    p.vec = reinterpret_cast<uintptr_t>(values) % 16 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0 ? 1 : 0;
+    p.N = num_values;
+    p.S = num_segments;
+    p.out = out;
+    p.tiles = tiles;
+    p.sm_count = ds->sm_count;
+    p.gen = sc->gen;
+    p.ticket = static_cast<unsigned long long*>(sc->ptr);
+    p.cta_aggf = reinterpret_cast<double*>(ws);
+    p.carryf = p.cta_aggf + RS_MAX_CTAS;
+    p.cta_first = reinterpret_cast<int64_t*>(p.carryf + RS_MAX_CTAS);
+    p.cta_aggi = reinterpret_cast<uint32_t*>(p.cta_first + RS_MAX_CTAS);
+    p.carryi = p.cta_aggi + RS_MAX_CTAS;
+    p.cta_flag = reinterpret_cast<int32_t*>(p.carryi + RS_MAX_CTAS);
+    p.bitmap = reinterpret_cast<unsigned long long*>(ws + cta_bytes);
+    if (launch_scan(p, stream) != cudaSuccess) {
         cudaGetLastError();
         return SEG_ERR_CUDA;
     }

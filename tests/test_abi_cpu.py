@@ -132,6 +132,24 @@ def test_scatter_host_checks_reject_before_any_cuda_call(lib):
     assert sc(64, 2, 1, -1, 64, 5, 0, 64, None, None) == 1          # N < 0
 
 
+def test_scan_host_checks_reject_before_any_cuda_call(lib):
+    # seg_scan(values, dtype, N, offsets, offsets_dtype, S, op, exclusive, out, stream)
+    sc = lib.seg_scan
+    assert sc(64, 2, 0, 64, 1, 3, 0, 0, 64, None) == 0             # N == 0: nothing to do
+    assert sc(64, 7, 10, 64, 1, 3, 0, 0, 64, None) == 1            # bad dtype
+    assert sc(64, 2, 10, 64, 5, 3, 0, 0, 64, None) == 1            # bad offsets dtype
+    assert sc(64, 2, 10, 64, 1, 3, 3, 0, 64, None) == 1            # mean is not a scan op
+    assert sc(64, 2, 10, 64, 1, 3, 2, 1, 64, None) == 2            # exclusive max
+    assert sc(64, 2, 10, 64, 1, 3, 0, 2, 64, None) == 1            # exclusive not 0 / 1
+    assert sc(64, 2, -1, 64, 1, 3, 0, 0, 64, None) == 1           # N < 0
+    assert sc(64, 2, 10, 64, 1, -1, 0, 0, 64, None) == 1           # S < 0
+    assert sc(None, 2, 10, 64, 1, 3, 0, 0, 64, None) == 1          # values NULL
+    assert sc(64, 2, 10, None, 1, 3, 0, 0, 64, None) == 1          # offsets NULL
+    assert sc(64, 2, 10, 64, 1, 3, 0, 0, None, None) == 1          # out NULL
+    assert sc(66, 2, 10, 64, 1, 3, 0, 0, 64, None) == 1            # values misaligned
+    assert sc(64, 2, 10, 68, 1, 3, 0, 0, 64, None) == 1            # int64 offsets misaligned
+
+
 def test_plan_shapes(lib):
     p = sr.plan("f32", 1, 16_000_000, "i64", 1_000_000, "sum", sm_count=152)
     assert p["grid"] == 152 and p["slot_threads"] == 1 and p["vec"] == 1
