@@ -74,12 +74,31 @@ __global__ void __launch_bounds__(RS_NT) rs_zero_kernel(unsigned long long* a, i
 }
 
 // One bit per offset inside [0, N): the row where a segment starts (the end
-// offset marks where the rows in no segment begin).
+// offset marks where the rows in no segment begin).  A thread takes
+// RS_FLAG_RUN consecutive offsets (sorted, so mostly in few words) and
+// issues one atomic OR per word it touches.
+constexpr int RS_FLAG_RUN = 8;
+
 __global__ void __launch_bounds__(RS_NT) rs_flag_kernel(const ScanParams p) {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * RS_NT;
-    for (int64_t s = static_cast<int64_t>(blockIdx.x) * RS_NT + threadIdx.x; s <= p.S; s += stride) {
-        const int64_t o = bound_at(p, s);
-        if (o < p.N) atomicOr(p.bitmap + (o >> 6), 1ull << (o & 63));
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * RS_NT * RS_FLAG_RUN;
+    for (int64_t s0 = (static_cast<int64_t>(blockIdx.x) * RS_NT + threadIdx.x) * RS_FLAG_RUN; s0 <= p.S;
+         s0 += stride) {
+        int64_t word = -1;
+        unsigned long long bits = 0;
+#pragma unroll
+        for (int k = 0; k < RS_FLAG_RUN; ++k) {
+            const int64_t s = s0 + k;
+            if (s > p.S) break;
+            const int64_t o = bound_at(p, s);
+            if (o >= p.N) break;   // nondecreasing: the rest are at N too
+            if ((o >> 6) != word) {
+                if (word >= 0) atomicOr(p.bitmap + word, bits);
+                word = o >> 6;
+                bits = 0;
+            }
+            bits |= 1ull << (o & 63);
+        }
+        if (word >= 0) atomicOr(p.bitmap + word, bits);
     }
 }
 
@@ -158,18 +177,21 @@ __global__ void __launch_bounds__(RS_NT) rs_scan_kernel(const ScanParams p) {
             ef = false;
             ev = id;
         }
-        // first start row of the tile, per warp
-        long long myfirst = cflags ? base + (__ffs(cflags) - 1) : LLONG_MAX;
+        // first start row of the tile, per warp (until the range's first is known)
+        const bool want_first = first == LLONG_MAX;
+        if (want_first) {
+            long long myfirst = cflags ? base + (__ffs(cflags) - 1) : LLONG_MAX;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const long long y = __shfl_xor_sync(0xffffffffu, myfirst, o);
-            myfirst = y < myfirst ? y : myfirst;
+            for (int o = 16; o > 0; o >>= 1) {
+                const long long y = __shfl_xor_sync(0xffffffffu, myfirst, o);
+                myfirst = y < myfirst ? y : myfirst;
+            }
+            if (lane == 0) s_wfirst[warp] = myfirst;
         }
         if (lane == 31) {
             s_wf[warp] = f;
             s_wv[warp] = v;
         }
-        if (lane == 0) s_wfirst[warp] = myfirst;
         __syncthreads();
         // the warps before mine, then the carry from the CTA's earlier tiles
         bool pf = false;
@@ -193,7 +215,7 @@ __global__ void __launch_bounds__(RS_NT) rs_scan_kernel(const ScanParams p) {
             combine<DT, OP>(tf, tv, f2, v2);
             tf = f2;
             tv = v2;
-            tfirst = s_wfirst[w] < tfirst ? s_wfirst[w] : tfirst;
+            if (want_first) tfirst = s_wfirst[w] < tfirst ? s_wfirst[w] : tfirst;
         }
         combine<DT, OP>(pf, pv, ef, ev);        // the warps before mine, then the lanes before me
         bool xf = ef;
@@ -217,9 +239,12 @@ __global__ void __launch_bounds__(RS_NT) rs_scan_kernel(const ScanParams p) {
                 prev = inc;
             }
         }
+        const int64_t tile0 = t * RS_TILE;
+        if (tile0 < lo || tile0 + RS_TILE > hi) {   // the tile reaches rows in no segment
 #pragma unroll
-        for (int j = 0; j < RS_PER; ++j)
-            if (base + j < lo || base + j >= hi) outv[j] = T(0);
+            for (int j = 0; j < RS_PER; ++j)
+                if (base + j < lo || base + j >= hi) outv[j] = T(0);
+        }
         T* out = static_cast<T*>(p.out) + base;
         if (p.vec && base + RS_PER <= p.N) {
 #pragma unroll
@@ -240,7 +265,7 @@ __global__ void __launch_bounds__(RS_NT) rs_scan_kernel(const ScanParams p) {
         combine<DT, OP>(cf, cv, tf, tv);
         cf = tf;
         cv = tv;
-        if (first == LLONG_MAX) first = tfirst;
+        if (want_first) first = tfirst;
         for (int j = 0; j < RS_PER; ++j) cur[j] = nxt[j];
         cflags = nflags;
         __syncthreads();
@@ -383,7 +408,7 @@ cudaError_t launch_op(ScanParams p, cudaStream_t stream) {
     p.ctas = static_cast<int32_t>(ctas < p.tiles ? ctas : p.tiles);
     const int64_t words = rs_bitmap_words(p.N);
     rs_zero_kernel<<<grid_for(words, RS_NT * 8), RS_NT, 0, stream>>>(p.bitmap, words);
-    rs_flag_kernel<<<grid_for(p.S + 1, RS_NT * 4), RS_NT, 0, stream>>>(p);
+    rs_flag_kernel<<<grid_for(p.S + 1, RS_NT * RS_FLAG_RUN), RS_NT, 0, stream>>>(p);
     rs_scan_kernel<DT, OP, EXCL><<<p.ctas, RS_NT, 0, stream>>>(p);
     rs_fix_kernel<DT, OP><<<static_cast<unsigned>(p.tiles), RS_NT, 0, stream>>>(p);
     return cudaGetLastError();
