@@ -5,8 +5,10 @@ case the workload lists (the scalar-bulk workload: uint32 / int32 / float32
 x sum / min+arg / max+arg), each one seg_reduce call = one kernel launch.
 
 value        algorithmic bytes of the step / summed CUDA-event kernel time,
-             inputs resident in HBM, L2 flushed (a 2 x L2 write) before
-             every call, outside the events.
+             inputs resident in HBM, L2 flushed before every call, outside
+             the events: a 2 x L2 write (no input line stays in L2), then a
+             2 x L2 read, so that the call starts from clean lines and does
+             not pay for writing back the flush's dirty ones.
 e2e          the same bytes / time of a step that copies its inputs from
              pinned host memory, runs the calls and copies the outputs back.
 roofline     the reduction kernel against the measured HBM copy bandwidth.
@@ -40,7 +42,9 @@ import workloads as W  # noqa: E402
 
 METRIC = "segmented-reduce effective HBM GB/s and % of GB300 peak; segments/s (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["ptx.cuh", "seg_common.cuh", "seg_rows2.cuh", "seg_scalar.cuh", "seg_pick.cuh", "api.cu"]
+# what shapes the reduction's launches: its kernels and its host planner
+KERNEL_SOURCES = ["ptx.cuh", "seg_common.cuh", "seg_rows2.cuh", "seg_scalar.cuh", "seg_pick.cuh",
+                  "seg_plan.cuh", "seg_f32.cu", "seg_u32.cu", "seg_s32.cu"]
 
 
 def kernel_hash() -> str:
@@ -73,6 +77,26 @@ def profile_traffic(config: str):
     if d.get("kernel_hash") != kernel_hash():
         return None
     return d.get("dram_bytes_per_launch")
+
+
+class L2Flush:
+    """Evict the inputs from L2 before a timed call: write a buffer of
+    2 x L2, then read another of 2 x L2, so that L2 holds clean lines that
+    belong to no input (the clean-cache state that ncu's cache control also
+    gives a profiled launch)."""
+
+    def __init__(self, dev):
+        import torch
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        n = max(2 * l2, 256 << 20) // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=dev)
+        self.r = torch.ones(n, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink)
 
 
 class ClockSampler:
@@ -260,7 +284,7 @@ def config_of(args, w):
       + ("; segmented scan (seg_scan), inclusive" if SCAN else ""),
         "segments": w.num_segments, "rows": w.num_rows, "features": w.feat,
         "cases": [f"{k}:{op}" for k, op in cases_of(w)],
-        "l2": "flushed before every timed call (2 x L2 write), outside the events"}
+        "l2": "flushed before every timed call (a 2 x L2 write, then a 2 x L2 read: clean lines), outside the events"}
 
 
 def run_ours(args, w: W.Workload):
@@ -294,8 +318,7 @@ def run_ours(args, w: W.Workload):
         o = torch.empty(shape, dtype=dvals[k].dtype, device=dev)
         a = torch.empty(shape, dtype=torch.int64, device=dev) if (op in ("min", "max") and not SCAN) else None
         outs[(k, op)] = (o, a)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     def call(k, op):
@@ -309,7 +332,7 @@ def run_ours(args, w: W.Workload):
 
     for _ in range(args.warmup):
         for k, op in cases:
-            flush.zero_()
+            flush()
             call(k, op)
     torch.cuda.synchronize(dev)
     assert sr.device_status(stream) == 0
@@ -326,7 +349,7 @@ def run_ours(args, w: W.Workload):
     n = 0
     for _ in range(args.steps):
         for k, op in cases:
-            flush.zero_()
+            flush()
             ev[n][0].record(stream)
             call(k, op)
             ev[n][1].record(stream)
@@ -447,7 +470,7 @@ def producer_config(args, w: W.Workload, n: int, runs: int):
     what = "segment-start flags (uint8)" if args.producer == "flags" else "ordered segment keys (uint32)"
     return {"workload": f"{args.producer} over the {what} of the {w.name} workload",
             "elements": n, "runs": runs, "producer": args.producer,
-            "l2": "flushed before every timed call (2 x L2 write), outside the events"}
+            "l2": "flushed before every timed call (a 2 x L2 write, then a 2 x L2 read: clean lines), outside the events"}
 
 
 def run_producer_reference(args, w: W.Workload):
@@ -511,10 +534,9 @@ def run_producer_ours(args, w: W.Workload):
             sr.seg_rle(dx, values=outs[0], lengths=outs[1], offsets=outs[2], count=c,
                        want_lengths=outs[1] is not None, want_offsets=outs[2] is not None)
 
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         call()
     torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -524,7 +546,7 @@ def run_producer_ours(args, w: W.Workload):
     clocks.start()
     time.sleep(0.3)
     for s, e in ev:
-        flush.zero_()
+        flush()
         s.record(stream)
         call()
         e.record(stream)
@@ -605,7 +627,7 @@ def scatter_config(args, n, feat, dim):
     return {"workload": f"scatter {args.config}: {n:,} float32 rows x {feat} into {dim:,} outputs, "
                         "destinations uniform, unsorted (graph-reduce README 'Measured' shape)",
             "rows": n, "features": feat, "outputs": dim, "cases": [f"f32:{op}" for op in SCATTER_CASES],
-            "l2": "flushed before every timed call (2 x L2 write), outside the events"}
+            "l2": "flushed before every timed call (a 2 x L2 write, then a 2 x L2 read: clean lines), outside the events"}
 
 
 def run_scatter_reference(args):
@@ -658,11 +680,10 @@ def run_scatter_ours(args):
         o, a = outs[op]
         sr.scatter(ds, di, dim, op, out=o, out_arg=a, with_arg=a is not None)
 
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     for _ in range(args.warmup):
         for op in SCATTER_CASES:
-            flush.zero_()
+            flush()
             call(op)
     torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -675,7 +696,7 @@ def run_scatter_ours(args):
     k = 0
     for _ in range(args.steps):
         for op in SCATTER_CASES:
-            flush.zero_()
+            flush()
             ev[k][0].record(stream)
             call(op)
             ev[k][1].record(stream)
