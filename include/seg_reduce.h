@@ -365,6 +365,20 @@ seg_status_t seg_rle(const uint32_t *keys, int64_t n, uint32_t *values, uint32_t
 seg_status_t seg_flags_to_offsets(const uint8_t *flags, int64_t n, int64_t *offsets,
                                   int64_t *count, seg_stream_t stream);
 
+/*
+ * seg_selftest_wait_timeout -- exercise the failure path of the bounded
+ * waits without a fault.  The kernels wait on mbarriers for their bulk
+ * copies with a time limit (2 s); a wait that runs out records
+ * SEG_ERR_DEVICE_TIMEOUT in the device status word (read by
+ * seg_reduce_device_status) and the kernel returns, so the context stays
+ * usable.  This call launches one thread that runs the same bounded wait on
+ * an mbarrier phase that nothing completes, with a limit of `limit_ms`
+ * milliseconds (1 .. 10000): after it, seg_reduce_device_status reports
+ * SEG_ERR_DEVICE_TIMEOUT once and the device keeps working.  The pages have
+ * no counterpart of this call; it exists for tests.
+ */
+seg_status_t seg_selftest_wait_timeout(uint32_t limit_ms, seg_stream_t stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t seg_reduce_version(void);
 

@@ -41,7 +41,8 @@ STATUS = {0: "SEG_OK", 1: "SEG_ERR_INVALID_ARGUMENT", 2: "SEG_ERR_UNSUPPORTED",
           6: "SEG_ERR_SCRATCH_LIMIT"}
 EXPORTED = ("seg_reduce", "seg_reduce_strerror", "seg_reduce_device_status",
             "seg_reduce_plan", "seg_reduce_version", "seg_reduce_noalloc", "seg_rle",
-            "seg_flags_to_offsets", "seg_reduce_sequential", "seg_scatter", "seg_scan")
+            "seg_flags_to_offsets", "seg_reduce_sequential", "seg_scatter", "seg_scan",
+            "seg_selftest_wait_timeout")
 NOALLOC_SCRATCH_BYTES = 2 << 20   # SEG_NOALLOC_SCRATCH_BYTES
 
 
@@ -98,6 +99,8 @@ def load_library(path: str | None = None):
         lib.seg_rle.argtypes = [vp, i64, vp, vp, vp, vp, vp]
         lib.seg_flags_to_offsets.restype = ctypes.c_int
         lib.seg_flags_to_offsets.argtypes = [vp, i64, vp, vp, vp]
+        lib.seg_selftest_wait_timeout.restype = ctypes.c_int
+        lib.seg_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         lib.seg_scan.restype = ctypes.c_int
         lib.seg_scan.argtypes = [vp, ctypes.c_int, i64, vp, ctypes.c_int, i64, ctypes.c_int, i32, vp, vp]
         lib.seg_scatter.restype = ctypes.c_int
@@ -529,6 +532,19 @@ def flags_to_offsets(flags):
     """``seg_flags_to_offsets`` trimmed to ``count + 1`` entries (synchronises)."""
     offsets, count = seg_flags_to_offsets(flags)
     return offsets[:int(count.item()) + 1]
+
+
+def selftest_wait_timeout(limit_ms: int = 50, stream=None) -> None:
+    """Launch the library's self-test of its bounded waits: a wait on a
+    phase that nothing completes, which runs out after ``limit_ms`` and
+    records a timeout in the device status word (read it with
+    ``device_status()``)."""
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    rc = load_library().seg_selftest_wait_timeout(limit_ms, ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SegReduceError(rc, "seg_selftest_wait_timeout")
 
 
 def device_status(stream=None) -> int:

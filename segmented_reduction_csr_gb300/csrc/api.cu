@@ -25,6 +25,17 @@ namespace {
 constexpr int32_t kVersion = 1 * 10000 + 0 * 100 + 0;
 constexpr int kMaxDevices = 64;
 
+// Self-test of the bounded waits: one thread waits, with the kernels' own
+// wait_bounded_for, on an mbarrier phase that nothing completes; the wait
+// runs out after limit_ns, ORs STATUS_CONSUMER_TIMEOUT into the status word
+// and the kernel returns.  No copy is in flight and nothing else waits.
+__global__ void selftest_wait_kernel(unsigned int* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+    (void)wait_bounded_for(&bar, 0, status, STATUS_CONSUMER_TIMEOUT, limit_ns);
+}
+
 // ---------------------------------------------------------------------------
 // Per-device state: SM count, status word, kernels already configured.
 
@@ -594,6 +605,24 @@ seg_status_t seg_scan(const void* values, seg_dtype_t dtype, int64_t num_values,
         cudaGetLastError();
         return SEG_ERR_CUDA;
     }
+    return SEG_OK;
+}
+
+seg_status_t seg_selftest_wait_timeout(uint32_t limit_ms, seg_stream_t stream_) {
+    if (limit_ms < 1 || limit_ms > 10000) return SEG_ERR_INVALID_ARGUMENT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SEG_ERR_CUDA;
+    unsigned int* status = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState* ds = nullptr;
+        const seg_status_t st = device_state(dev, &ds);
+        if (st != SEG_OK) return st;
+        status = ds->status;
+    }
+    selftest_wait_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(
+        status, static_cast<uint64_t>(limit_ms) * 1000000ull);
+    if (cudaGetLastError() != cudaSuccess) return SEG_ERR_CUDA;
     return SEG_OK;
 }
 

@@ -281,18 +281,23 @@ __device__ __forceinline__ void issue_chunk(const Stream& s, int64_t m, unsigned
 }
 
 // Wait for a phase with a time limit; records `code` in the status word on expiry.
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, unsigned int* status,
-                                             unsigned code) {
+__device__ __forceinline__ bool wait_bounded_for(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                                 unsigned code, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         for (int k = 0; k < 8; ++k)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             atomicOr(status, code);
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                             unsigned code) {
+    return wait_bounded_for(bar, parity, status, code, WAIT_LIMIT_NS);
 }
 
 template <class OffT>
