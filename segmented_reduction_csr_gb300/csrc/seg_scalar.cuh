@@ -58,7 +58,7 @@ constexpr int SW_NDIAG = SW_NW + 1;            // unit boundaries per CTA
 constexpr int SW_GRID = 1024;                  // first-round probes, shared by all CTAs
 constexpr int SW_PROBES = 60;                  // later-round probes per boundary
 static_assert(SW_Q % 2 == 1, "conflict-free 128-bit row loads need SW_KR / 4 odd");
-static_assert(SW_NDIAG * SW_PROBES <= 2 * SW_NTHREADS, "two probes per thread per round");
+constexpr int SW_PROBE_PASSES = (SW_NDIAG * SW_PROBES + SW_NTHREADS - 1) / SW_NTHREADS;   // per thread per round
 static_assert(SW_EMAXT % 32 == 0, "ends are taken 32 at a time");
 
 // Per-warp shared memory.
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     __syncthreads();
     for (int round = 0; round < 64; ++round) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < SW_PROBE_PASSES; ++u) {
             const int pidx = tid + u * SW_NTHREADS;
             const int k = pidx / SW_PROBES;
             const int mm = pidx - k * SW_PROBES;
