@@ -288,7 +288,6 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     const bool want_arg = (OP != OP_SUM) && p.out_arg != nullptr;
 
     const uint64_t vbase = reinterpret_cast<uint64_t>(p.values);
-    const uint64_t obase = reinterpret_cast<uint64_t>(p.offsets);
     const Stream vs = make_stream(vbase, static_cast<uint64_t>(N) * 4, vbase + Ru * 4, vbase + Ru2 * 4,
                                   SW_VCHUNK);
     const int32_t nR = static_cast<int32_t>(Ru2 - Ru);
