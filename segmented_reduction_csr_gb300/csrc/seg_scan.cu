@@ -126,7 +126,9 @@ __device__ __forceinline__ void load_tile(const ScanParams& p, int64_t base, typ
         for (int j = 0; j < RS_PER; ++j)
             v[j] = base + j < p.N ? __ldg(static_cast<const T*>(p.values) + base + j) : T(0);
     }
-    flags = base < p.N ? static_cast<uint32_t>((__ldcg(p.bitmap + (base >> 6)) >> (base & 63)) & 0xffffull) : 0u;
+    static_assert(RS_PER == 8 || RS_PER == 16 || RS_PER == 32, "a thread's start bits lie in one bitmap word");
+    constexpr unsigned long long kMask = (1ull << RS_PER) - 1;
+    flags = base < p.N ? static_cast<uint32_t>((__ldcg(p.bitmap + (base >> 6)) >> (base & 63)) & kMask) : 0u;
 }
 
 // Scan pass: CTA b scans its tiles in order, carrying the open segment.

@@ -28,9 +28,9 @@
 
 namespace segred {
 
-constexpr int RS_NT = 256;
+constexpr int RS_NT = 128;
 constexpr int RS_PER = 16;
-constexpr int RS_TILE = RS_NT * RS_PER;    // 4,096 rows
+constexpr int RS_TILE = RS_NT * RS_PER;    // 2,048 rows
 constexpr int RS_MAX_CTAS = 1024;
 
 struct ScanParams {
