@@ -13,6 +13,17 @@ segment ``s`` reduces rows ``[indptr[s], indptr[s+1])`` of ``src`` (``[N]`` or
 and float32, ``mean`` for float32; ``min`` / ``max`` also return the absolute
 source row (int64; ties to the lower row; -1 for an empty segment); empty
 segments give 0.
+
+Beside the reduction (``seg_reduce``, ``segment_*_csr``, ``seg_reduce_noalloc``):
+
+* ``seg_reduce_sequential``: float32 sum / mean added in input order
+  (bitwise equal to an in-order float32 loop, as torch.segment_reduce);
+* ``scatter`` / ``scatter_{sum,add,mean,max,min}``: the unsorted path, one
+  atomic per element (graph-reduce README "API");
+* ``seg_scan`` / ``segment_cumsum_csr``: segmented inclusive / exclusive scan;
+* ``seg_rle`` / ``rle`` / ``unique`` and ``seg_flags_to_offsets`` /
+  ``flags_to_offsets``: producers of offsets (GPURunLengthEncode, GPUUnique,
+  GPUSegmentedLayout).
 """
 from __future__ import annotations
 
