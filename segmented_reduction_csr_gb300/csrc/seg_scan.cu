@@ -133,7 +133,7 @@ __device__ __forceinline__ void load_tile(const ScanParams& p, int64_t base, typ
 
 // Scan pass: CTA b scans its tiles in order, carrying the open segment.
 template <int DT, int OP, bool EXCL>
-__global__ void __launch_bounds__(RS_NT) rs_scan_kernel(const ScanParams p) {
+__global__ void __launch_bounds__(RS_NT, 8) rs_scan_kernel(const ScanParams p) {
     using T = typename ScanType<DT>::T;
     __shared__ T s_wv[kWarps];
     __shared__ int s_wf[kWarps];

@@ -33,20 +33,23 @@ __global__ void __launch_bounds__(SC_NT) sc_add_kernel(const ScatterParams p) {
         const int64_t it = first + static_cast<int64_t>(k) * SC_NT;
         dst[k] = -1;
         if (it < items) {
+            // the row's values load whatever its index says (the row is in
+            // bounds), so the two loads overlap instead of one waiting on the other
             const int64_t r = it / chunks, c = it - r * chunks;
-            const int64_t d = __ldg(p.index + r);
+            dst[k] = __ldg(p.index + r);
             col[k] = c * VEC;
-            if (d >= 0 && d < p.D) {
-                dst[k] = d;
-                if constexpr (DT == 2 && VEC == 4)
-                    fv[k] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.src) + r * p.F) + c);
-                else if constexpr (DT == 2)
-                    fv[k].x = __ldg(static_cast<const float*>(p.src) + r * p.F + c);
-                else
-                    iv[k] = __ldg(static_cast<const uint32_t*>(p.src) + r * p.F + c);
-                if (p.count != nullptr && c == 0) atomicAdd(p.count + d, 1u);
-            }
+            if constexpr (DT == 2 && VEC == 4)
+                fv[k] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.src) + r * p.F) + c);
+            else if constexpr (DT == 2)
+                fv[k].x = __ldg(static_cast<const float*>(p.src) + r * p.F + c);
+            else
+                iv[k] = __ldg(static_cast<const uint32_t*>(p.src) + r * p.F + c);
         }
+    }
+#pragma unroll
+    for (int k = 0; k < SC_ITEMS; ++k) {
+        if (dst[k] >= p.D) dst[k] = -1;   // outside [0, D): the row goes nowhere
+        if (p.count != nullptr && dst[k] >= 0 && col[k] == 0) atomicAdd(p.count + dst[k], 1u);
     }
 #pragma unroll
     for (int k = 0; k < SC_ITEMS; ++k) {
@@ -85,14 +88,13 @@ __global__ void __launch_bounds__(SC_NT) sc_ext_kernel(const ScatterParams p) {
         const int64_t it = first + static_cast<int64_t>(k) * SC_NT;
         cell[k] = -1;
         if (it < items) {
+            // value and index load together (the row is in bounds either way)
             const int64_t r = it / p.F, c = it - r * p.F;
             const int64_t d = __ldg(p.index + r);
-            if (d >= 0 && d < p.D) {
-                const uint32_t bits = __ldg(static_cast<const uint32_t*>(p.src) + it);
-                const uint32_t lo = MAX ? ~static_cast<uint32_t>(r) : static_cast<uint32_t>(r);
-                w[k] = (static_cast<unsigned long long>(monotone<DT>(bits)) << 32) | lo;
-                cell[k] = d * p.F + c;
-            }
+            const uint32_t bits = __ldg(static_cast<const uint32_t*>(p.src) + it);
+            const uint32_t lo = MAX ? ~static_cast<uint32_t>(r) : static_cast<uint32_t>(r);
+            w[k] = (static_cast<unsigned long long>(monotone<DT>(bits)) << 32) | lo;
+            cell[k] = d >= 0 && d < p.D ? d * p.F + c : -1;
         }
     }
 #pragma unroll
