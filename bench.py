@@ -649,8 +649,10 @@ def scatter_bytes(n: int, feat: int, dim: int, op: str) -> int:
 
 
 def scatter_config(args, n, feat, dim):
+    mode = ("; deterministic: stable sort by destination, then the segmented path"
+            if getattr(args, "deterministic", False) else "; atomics")
     return {"workload": f"scatter {args.config}: {n:,} float32 rows x {feat} into {dim:,} outputs, "
-                        "destinations uniform, unsorted (graph-reduce README 'Measured' shape)",
+                        "destinations uniform, unsorted (graph-reduce README 'Measured' shape)" + mode,
             "rows": n, "features": feat, "outputs": dim, "cases": [f"f32:{op}" for op in SCATTER_CASES],
             "l2": "flushed before every timed call (a 2 x L2 write, then a 2 x L2 read: clean lines), outside the events"}
 
@@ -703,7 +705,8 @@ def run_scatter_ours(args):
 
     def call(op):
         o, a = outs[op]
-        sr.scatter(ds, di, dim, op, out=o, out_arg=a, with_arg=a is not None)
+        sr.scatter(ds, di, dim, op, out=o, out_arg=a, with_arg=a is not None,
+                   deterministic=args.deterministic)
 
     flush = L2Flush(dev)
     for _ in range(args.warmup):
@@ -762,7 +765,8 @@ def run_scatter_ours(args):
     d2h = sum(o.numel() * 4 + (a.numel() * 8 if a is not None else 0) for o, a in host_out.values())
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = run_scatter_reference(argparse.Namespace(steps=1, warmup=0, gpus=1, config=args.config))["cpu_baseline"]
+        cpu = run_scatter_reference(argparse.Namespace(steps=1, warmup=0, gpus=1, config=args.config,
+                                                       deterministic=args.deterministic))["cpu_baseline"]
     peak, peak_kind = measured_peak()
     achieved = nbytes * args.steps / (sum(per_call) * 1e-3) / 1e9
     line = {
@@ -773,11 +777,14 @@ def run_scatter_ours(args):
         "config": scatter_config(args, n, feat, dim),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
-                     "kernel": "segred::sc_add_kernel / sc_ext_kernel with their fill and finishing launches",
+                     "kernel": ("segred sort (histogram, scan, scatter passes), gather and seg_reduce launches"
+                                if args.deterministic else
+                                "segred::sc_add_kernel / sc_ext_kernel with their fill and finishing launches"),
                      "peak_note": f"{peak_kind} HBM copy bandwidth"},
         "e2e": {"value": whole_job_gbs(world, nbytes, args.steps, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": int(hs.numel() * 4 + hi.numel() * 8), "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (2 + 3 + 3),
+        "gpu_launches": args.steps * (2 + 3 + 3 if not args.deterministic else
+                                      3 * (3 * ((int(dim).bit_length() + 7) // 8) + 3) + 1),
         "clocks": clk,
         "breakdown": breakdown,
     }
@@ -799,6 +806,8 @@ def main():
     ap.add_argument("--producer", default=None, choices=["rle", "unique", "flags"])
     ap.add_argument("--scatter", action="store_true",
                     help="time the unsorted scatter path (sum, mean, max) on the mp or mp16 shape")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="with --scatter: the sorted, bitwise reproducible scatter")
     ap.add_argument("--scan", action="store_true",
                     help="time the segmented scan (inclusive float32 sum and max) instead")
     ap.add_argument("--sequential", action="store_true",

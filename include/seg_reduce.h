@@ -274,6 +274,34 @@ seg_status_t seg_scatter(const void *src, seg_dtype_t dtype, int64_t F, int64_t 
                          int64_t *out_arg, seg_stream_t stream);
 
 /*
+ * seg_scatter_sorted -- the scatter path made deterministic: the same
+ * results as seg_scatter (same arguments, same readings), but float32 sums
+ * and means are bitwise reproducible.
+ *
+ * graph-reduce README (HF kernels hub), "Correctness": the atomic scatter's
+ * order is not fixed, the CSR path's is; and "Usage": rows sorted by
+ * destination, with the pointer built from the destination counts, go
+ * through the CSR path.  This call does that on the device: a stable radix
+ * sort of the rows by destination (an index outside [0, dim_size) sorts
+ * last and is left out), the offsets of each destination's rows, a gather
+ * of the rows in sorted order, seg_reduce over them, and the args of
+ * max / min mapped back to src's rows.  Within a destination the rows keep
+ * their order, so the result equals, bit for bit, seg_reduce over all of
+ * src's rows stably sorted by destination (an index outside [0, dim_size)
+ * taken as dim_size) with the offsets of the destinations' counts.
+ *
+ * Arguments as for seg_scatter; num_rows and dim_size below 2^32 - 1.
+ * Scratch: a buffer of its own per (device, stream) of about 16 bytes per row
+ * plus num_rows * F * 4 bytes for the gathered rows plus 8 bytes per output
+ * row; seg_reduce uses its own.  Enqueues the sort (three launches per 8 bits
+ * of dim_size), three more launches and seg_reduce's, and returns without
+ * synchronising.
+ */
+seg_status_t seg_scatter_sorted(const void *src, seg_dtype_t dtype, int64_t F, int64_t num_rows,
+                                const int64_t *index, int64_t dim_size, seg_op_t op, void *out,
+                                int64_t *out_arg, seg_stream_t stream);
+
+/*
  * seg_reduce_sequential -- the input-order float32 mode of the sum and mean.
  *
  * graph-reduce README (HF kernels hub), "Correctness": its CSR path is

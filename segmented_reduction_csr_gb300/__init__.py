@@ -52,7 +52,7 @@ STATUS = {0: "SEG_OK", 1: "SEG_ERR_INVALID_ARGUMENT", 2: "SEG_ERR_UNSUPPORTED",
           6: "SEG_ERR_SCRATCH_LIMIT"}
 EXPORTED = ("seg_reduce", "seg_reduce_strerror", "seg_reduce_device_status",
             "seg_reduce_plan", "seg_reduce_version", "seg_reduce_noalloc", "seg_rle",
-            "seg_flags_to_offsets", "seg_reduce_sequential", "seg_scatter", "seg_scan",
+            "seg_flags_to_offsets", "seg_reduce_sequential", "seg_scatter", "seg_scatter_sorted", "seg_scan",
             "seg_selftest_wait_timeout")
 NOALLOC_SCRATCH_BYTES = 2 << 20   # SEG_NOALLOC_SCRATCH_BYTES
 
@@ -114,6 +114,8 @@ def load_library(path: str | None = None):
         lib.seg_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         lib.seg_scan.restype = ctypes.c_int
         lib.seg_scan.argtypes = [vp, ctypes.c_int, i64, vp, ctypes.c_int, i64, ctypes.c_int, i32, vp, vp]
+        lib.seg_scatter_sorted.restype = ctypes.c_int
+        lib.seg_scatter_sorted.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp]
         lib.seg_scatter.restype = ctypes.c_int
         lib.seg_scatter.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp]
         lib.seg_reduce_sequential.restype = ctypes.c_int
@@ -337,15 +339,17 @@ def segment_cumsum_csr(src, indptr):
 
 
 def scatter(src, index, dim_size: int, reduce: str = "sum", out=None, out_arg=None,
-            with_arg: bool = True, stream=None):
+            with_arg: bool = True, deterministic: bool = False, stream=None):
     """Scatter the rows of ``src`` ([N] or [N, F], CUDA) into ``dim_size``
     outputs named by ``index`` ([N] int64, CUDA) -- graph-reduce README,
     "API": ``sum`` (or ``add``), ``mean`` (float32; 0 where nothing arrived),
     ``max`` / ``min`` returning ``(values, arg)`` (the lowest row holding the
     extreme; 0 and -1 where nothing arrived).  A row whose index is outside
     [0, dim_size) goes nowhere.  float32 sums and means use atomics and are
-    not bitwise reproducible; use the segmented path (sorted rows and
-    ``seg_reduce``) when they must be.  Not synchronised."""
+    not bitwise reproducible unless ``deterministic``: then the rows are
+    stably sorted by destination on the device and reduced by the segmented
+    path (``seg_scatter_sorted``), so every result repeats bit for bit, at
+    the cost of the sort and a gather.  Not synchronised."""
     torch = _torch()
     op = "sum" if reduce == "add" else reduce
     if op not in OPS:
@@ -373,14 +377,15 @@ def scatter(src, index, dim_size: int, reduce: str = "sum", out=None, out_arg=No
     lib = load_library()
     if stream is None:
         stream = torch.cuda.current_stream(src.device)
+    fn = lib.seg_scatter_sorted if deterministic else lib.seg_scatter
     with torch.cuda.device(src.device):
-        rc = lib.seg_scatter(src.data_ptr() if n else None, _value_code(src), feat, n,
-                             index.data_ptr() if n else None, dim_size, OPS[op],
-                             out.data_ptr() if dim_size else None,
-                             out_arg.data_ptr() if (want_arg and dim_size) else None,
-                             ctypes.c_void_p(stream.cuda_stream))
+        rc = fn(src.data_ptr() if n else None, _value_code(src), feat, n,
+                index.data_ptr() if n else None, dim_size, OPS[op],
+                out.data_ptr() if dim_size else None,
+                out_arg.data_ptr() if (want_arg and dim_size) else None,
+                ctypes.c_void_p(stream.cuda_stream))
     if rc != 0:
-        raise SegReduceError(rc, "seg_scatter")
+        raise SegReduceError(rc, "seg_scatter_sorted" if deterministic else "seg_scatter")
     return (out, out_arg) if want_arg else out
 
 

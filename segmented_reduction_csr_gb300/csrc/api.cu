@@ -17,6 +17,7 @@
 #include "seg_scan.cuh"
 #include "seg_scatter.cuh"
 #include "seg_seq.cuh"
+#include "seg_sort.cuh"
 
 using namespace segred;
 
@@ -55,6 +56,10 @@ struct Scratch {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
+// The deterministic scatter's sort buffers, offsets and gathered rows: a
+// buffer of their own per (device, stream), so that the reduction it runs
+// keeps its scratch (and its ticket words) to itself.
+std::map<std::pair<int, cudaStream_t>, Scratch> g_sort_scratch;
 
 seg_status_t device_state(int dev, DeviceState** out) {
     if (dev < 0 || dev >= kMaxDevices) return SEG_ERR_CUDA;
@@ -79,8 +84,9 @@ seg_status_t device_state(int dev, DeviceState** out) {
 
 // Scratch for (device, stream): grown on demand, zeroed when (re)allocated,
 // stream-ordered so earlier work on the stream still sees the old buffer.
-seg_status_t scratch_for(int dev, cudaStream_t stream, size_t bytes, Scratch** out) {
-    Scratch& sc = g_scratch[std::make_pair(dev, stream)];
+seg_status_t scratch_in(std::map<std::pair<int, cudaStream_t>, Scratch>& cache, int dev,
+                        cudaStream_t stream, size_t bytes, Scratch** out) {
+    Scratch& sc = cache[std::make_pair(dev, stream)];
     if (sc.bytes < bytes || sc.gen == UINT32_MAX) {
         size_t want = std::max<size_t>(bytes, size_t(1) << 20);
         want = std::max(want, sc.bytes);
@@ -98,6 +104,10 @@ seg_status_t scratch_for(int dev, cudaStream_t stream, size_t bytes, Scratch** o
     }
     *out = &sc;
     return SEG_OK;
+}
+
+seg_status_t scratch_for(int dev, cudaStream_t stream, size_t bytes, Scratch** out) {
+    return scratch_in(g_scratch, dev, stream, bytes, out);
 }
 
 // ---------------------------------------------------------------------------
@@ -540,6 +550,79 @@ seg_status_t seg_scatter(const void* src, seg_dtype_t dtype, int64_t F, int64_t 
     if (launch_scatter(p, stream) != cudaSuccess) {
         cudaGetLastError();
         return SEG_ERR_CUDA;
+    }
+    return SEG_OK;
+}
+
+seg_status_t seg_scatter_sorted(const void* src, seg_dtype_t dtype, int64_t F, int64_t num_rows,
+                                const int64_t* index, int64_t dim_size, seg_op_t op, void* out,
+                                int64_t* out_arg, seg_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (dtype != SEG_U32 && dtype != SEG_S32 && dtype != SEG_F32) return SEG_ERR_INVALID_ARGUMENT;
+    if (op != SEG_SUM && op != SEG_MIN && op != SEG_MAX && op != SEG_MEAN) return SEG_ERR_INVALID_ARGUMENT;
+    if (F < 1 || num_rows < 0 || dim_size < 0) return SEG_ERR_INVALID_ARGUMENT;
+    if (op == SEG_MEAN && dtype != SEG_F32) return SEG_ERR_UNSUPPORTED;
+    if (F > SEG_MAX_FEATURES) return SEG_ERR_UNSUPPORTED;
+    if ((op == SEG_SUM || op == SEG_MEAN) && out_arg != nullptr) return SEG_ERR_INVALID_ARGUMENT;
+    // row numbers and keys are 32-bit
+    if (num_rows >= int64_t(UINT32_MAX) || dim_size >= int64_t(UINT32_MAX)) return SEG_ERR_UNSUPPORTED;
+    if (dim_size == 0) return SEG_OK;
+    if (!out || (num_rows > 0 && (!src || !index))) return SEG_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(src) % 4 || reinterpret_cast<uintptr_t>(out) % 4 ||
+        reinterpret_cast<uintptr_t>(index) % 8 || reinterpret_cast<uintptr_t>(out_arg) % 8)
+        return SEG_ERR_INVALID_ARGUMENT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SEG_ERR_CUDA;
+    SortParams sp{};
+    int64_t* offsets = nullptr;
+    void* rows = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState* ds = nullptr;
+        seg_status_t st = device_state(dev, &ds);
+        if (st != SEG_OK) return st;
+        // sort buffers, then offsets, then the gathered rows
+        const int64_t sort_bytes = ceil_div(sort_scratch_bytes(num_rows), 256) * 256;
+        const int64_t off_bytes = ceil_div((dim_size + 1) * 8, 256) * 256;
+        const int64_t row_bytes = num_rows * F * 4;
+        Scratch* sc = nullptr;
+        st = scratch_in(g_sort_scratch, dev, stream, static_cast<size_t>(sort_bytes + off_bytes + row_bytes), &sc);
+        if (st != SEG_OK) return st;
+        unsigned char* ws = static_cast<unsigned char*>(sc->ptr);
+        sp.index = index;
+        sp.N = num_rows;
+        sp.D = dim_size;
+        sp.tiles = ceil_div(num_rows, SORT_TILE);
+        for (int b = 0; b < 2; ++b) {
+            sp.keys[b] = reinterpret_cast<uint32_t*>(ws) + b * num_rows;
+            sp.vals[b] = reinterpret_cast<uint32_t*>(ws) + (2 + b) * num_rows;
+        }
+        sp.hist = reinterpret_cast<uint32_t*>(ws) + 4 * num_rows;
+        sp.total = sp.hist + int64_t(SORT_RADIX) * sp.tiles;
+        int bits = 0;
+        for (int64_t d = dim_size; d > 0; d >>= 1) ++bits;   // keys go up to dim_size
+        sp.passes = (bits + 7) / 8;
+        offsets = reinterpret_cast<int64_t*>(ws + sort_bytes);
+        rows = ws + sort_bytes + off_bytes;
+        const uint32_t* sorted = sp.keys[(sp.passes - 1) & 1];
+        const uint32_t* perm = sp.vals[(sp.passes - 1) & 1];
+        if (launch_sort(sp, stream) != cudaSuccess ||
+            launch_bucket_offsets(sorted, num_rows, dim_size, offsets, stream) != cudaSuccess ||
+            launch_gather_rows(src, perm, num_rows, F, rows, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return SEG_ERR_CUDA;
+        }
+    }
+    // the groups are contiguous now: the deterministic segmented reduction
+    const seg_status_t st = seg_reduce(num_rows > 0 ? rows : nullptr, dtype, F, num_rows, offsets, SEG_OFF_I64,
+                                       dim_size, op, out, out_arg, stream_);
+    if (st != SEG_OK) return st;
+    if (out_arg != nullptr && (op == SEG_MIN || op == SEG_MAX) && num_rows > 0) {
+        // args name rows of the sorted copy: map them back to src's rows
+        if (launch_map_args(out_arg, sp.vals[(sp.passes - 1) & 1], dim_size * F, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return SEG_ERR_CUDA;
+        }
     }
     return SEG_OK;
 }

@@ -132,6 +132,19 @@ def test_scatter_host_checks_reject_before_any_cuda_call(lib):
     assert sc(64, 2, 1, -1, 64, 5, 0, 64, None, None) == 1          # N < 0
 
 
+def test_sorted_scatter_host_checks_reject_before_any_cuda_call(lib):
+    sc = lib.seg_scatter_sorted
+    assert sc(64, 2, 1, 10, 64, 0, 0, 64, None, None) == 0          # dim_size 0: nothing to do
+    assert sc(64, 7, 1, 10, 64, 5, 0, 64, None, None) == 1          # bad dtype
+    assert sc(64, 2, 1, 10, 64, 5, 9, 64, None, None) == 1          # bad op
+    assert sc(64, 0, 1, 10, 64, 5, 3, 64, None, None) == 2          # mean on uint32
+    assert sc(64, 2, 1, 10, 64, 5, 0, 64, 64, None) == 1            # arg with sum
+    assert sc(64, 2, 1, 1 << 32, 64, 5, 2, 64, None, None) == 2     # rows do not fit 32 bits
+    assert sc(64, 2, 1, 10, 64, 1 << 32, 2, 64, None, None) == 2    # outputs do not fit 32 bits
+    assert sc(None, 2, 1, 10, 64, 5, 0, 64, None, None) == 1        # src NULL
+    assert sc(64, 2, 1, 10, 68, 5, 0, 64, None, None) == 1          # index misaligned
+
+
 def test_scan_host_checks_reject_before_any_cuda_call(lib):
     # seg_scan(values, dtype, N, offsets, offsets_dtype, S, op, exclusive, out, stream)
     sc = lib.seg_scan

@@ -134,3 +134,77 @@ def test_integer_and_extreme_results_repeat_exactly(sr):
             again = sr.scatter(dv, idx, 123, op)
             again = again[0] if isinstance(again, tuple) else again
             assert torch.equal(first, again), op
+
+
+# ---- the deterministic scatter (sort by destination, then the segmented path) ----------
+
+def _sorted_reference(sr, v, idx, dim, op):
+    """seg_reduce over all rows stably sorted on the host by destination (an
+    index outside [0, dim) taken as dim, so those rows sort last and lie in
+    no segment), args mapped back to the original rows.  All N rows stay in
+    the array: the reduction's fixed float order depends on its row count."""
+    ok = (idx >= 0) & (idx < dim)
+    key = np.where(ok, idx, dim)
+    perm = np.argsort(key, kind="stable")
+    off = np.concatenate([[0], np.cumsum(np.bincount(idx[ok], minlength=dim))]).astype(np.int64)
+    r = sr.seg_reduce(to_dev(np.ascontiguousarray(v[perm])), to_dev(off), op)
+    if isinstance(r, tuple):
+        o, a = to_host(r[0]), to_host(r[1])
+        return o, np.where(a >= 0, perm[np.maximum(a, 0)], -1)
+    return to_host(r), None
+
+
+@pytest.mark.parametrize("dim", [1, 300, 70_000])
+@pytest.mark.parametrize("feat", [1, 8, 64])
+def test_sorted_scatter_equals_segmented_path_over_sorted_rows(sr, dim, feat):
+    """Bit for bit: the device sort is stable and the reduction is the
+    segmented path's (1, 2 and 3 radix passes)."""
+    rng = np.random.default_rng(dim + feat)
+    n = 50_003
+    v = rng.standard_normal((n,) if feat == 1 else (n, feat)).astype(np.float32)
+    idx = rng.integers(-3, dim + 3, size=n).astype(np.int64)
+    for op in ("sum", "mean", "max", "min"):
+        got = sr.scatter(to_dev(v), to_dev(idx), dim, op, deterministic=True)
+        exp, exp_arg = _sorted_reference(sr, v, idx, dim, op)
+        if isinstance(got, tuple):
+            assert np.array_equal(to_host(got[0]).view(np.uint32), exp.view(np.uint32)), op
+            assert np.array_equal(to_host(got[1]), exp_arg), op
+        else:
+            assert np.array_equal(to_host(got).view(np.uint32), exp.view(np.uint32)), op
+
+
+@pytest.mark.parametrize("kind", ["u32", "s32", "f32"])
+def test_sorted_scatter_against_the_oracle(sr, kind):
+    rng = np.random.default_rng(7 + len(kind))
+    v = _values(rng, kind, (40_000, 5))
+    idx = rng.integers(0, 777, size=40_000).astype(np.int64)
+    for op in ("sum", "max", "min") + (("mean",) if kind == "f32" else ()):
+        exp = oracle.scatter(v, idx, 777, op)
+        got = sr.scatter(to_dev(v), to_dev(idx), 777, op, deterministic=True)
+        if op in ("max", "min"):
+            assert np.array_equal(to_host(got[0]).view(np.uint32), exp[0].view(np.uint32)), op
+            assert np.array_equal(to_host(got[1]), exp[1]), op
+        elif kind != "f32":
+            assert np.array_equal(to_host(got), exp), op
+        else:
+            err = np.abs(to_host(got).astype(np.float64) - exp.astype(np.float64))
+            tol = TOL_REL * _abs_sums(v, idx, 777) + TOL_ABS
+            if op == "mean":
+                cnt = np.bincount(idx, minlength=777).astype(np.float64)[:, None]
+                tol = tol / np.maximum(cnt, 1) + np.abs(exp.astype(np.float64)) * 2.0 ** -23
+            assert np.all(err <= tol), op
+
+
+def test_sorted_scatter_is_bitwise_reproducible_and_handles_no_rows(sr):
+    import torch
+    v, idx, dim = W.scatter_input("mp")
+    dv, di = to_dev(v), to_dev(idx)
+    first = sr.scatter(dv, di, dim, "sum", deterministic=True).clone()
+    for _ in range(3):
+        again = sr.scatter(dv, di, dim, "sum", deterministic=True)
+        assert torch.equal(again.view(torch.int32), first.view(torch.int32))
+    exp, _ = _sorted_reference(sr, v, idx, dim, "sum")
+    assert np.array_equal(to_host(first).view(np.uint32), exp.view(np.uint32))
+    o, a = sr.scatter(torch.zeros((0, 4), dtype=torch.float32, device="cuda"),
+                      torch.zeros(0, dtype=torch.int64, device="cuda"), 5, "max", deterministic=True)
+    assert not to_host(o).any() and (to_host(a) == -1).all()
