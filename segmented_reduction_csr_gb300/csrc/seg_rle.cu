@@ -231,8 +231,25 @@ __global__ void __launch_bounds__(RLE_NT) rle_count_kernel(const RleParams p) {
 // writing slots 64 t + j) free of bank conflicts.
 __device__ __forceinline__ int rel_slot(int k) { return k + 2 * (k >> 6); }
 
+// The count CTA b whose range [t0, t1) holds tile t (the inverse of
+// cta_tiles).  Below 2^21 tiles every product fits 32 bits and the divisions
+// are 32-bit ones.
+__device__ __forceinline__ void owner_of(const RleParams& p, int64_t t, int64_t& b, int64_t& t0, int64_t& t1) {
+    if (p.tiles < (int64_t(1) << 21)) {
+        const uint32_t T = static_cast<uint32_t>(p.tiles), C = static_cast<uint32_t>(p.ctas);
+        const uint32_t bb = ((static_cast<uint32_t>(t) + 1) * C + T - 1) / T - 1;
+        b = bb;
+        t0 = T * bb / C;
+        t1 = T * (bb + 1) / C;
+    } else {
+        b = ((t + 1) * p.ctas + p.tiles - 1) / p.tiles - 1;
+        t0 = p.tiles * b / p.ctas;
+        t1 = p.tiles * (b + 1) / p.ctas;
+    }
+}
+
 // CTA t writes the runs that start in tile t.  Thread i owns bitmap word i:
-// elements tile0 + 64 i + [0, 64).
+// elements tile0 + 64 i + [0, 64).  A tile without starts returns at once.
 __global__ void __launch_bounds__(RLE_NT) rle_write_kernel(const RleParams p) {
     __shared__ uint16_t s_rel[RLE_TILE + 2 * (RLE_TILE / 64) + 2];
     __shared__ int s_warp[kWarps];
@@ -240,11 +257,11 @@ __global__ void __launch_bounds__(RLE_NT) rle_write_kernel(const RleParams p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = blockIdx.x;
     const int64_t tile0 = t * RLE_TILE;
+    if (__ldcg(p.tile_count + t) == 0) return;
     const unsigned long long word = __ldcg(p.bitmap + t * RLE_NT + threadIdx.x);
     if (warp == 0) {
-        // the count CTA b whose range [t0, t1) holds tile t
-        const int64_t b = ((t + 1) * p.ctas + p.tiles - 1) / p.tiles - 1;
-        const int64_t t0 = p.tiles * b / p.ctas, t1 = p.tiles * (b + 1) / p.ctas;
+        int64_t b, t0, t1;
+        owner_of(p, t, b, t0, t1);
         const int64_t b_run = __ldcg(p.cta_base + b), b_after = __ldcg(p.cta_next + b);
         // runs before the tile: b's base plus the starts of b's tiles before t;
         // the first start after the tile: in b's later tiles, else after b
