@@ -250,7 +250,8 @@ seg_status_t seg_scan(const void *values, seg_dtype_t dtype, int64_t num_values,
  *              enables 128-bit float32 vector reductions).
  *   dtype      SEG_U32, SEG_S32 or SEG_F32.
  *   F          columns, 1 <= F <= SEG_MAX_FEATURES.
- *   num_rows   N, 0 <= N < 2^32 - 1 (rows are packed into 32 bits).
+ *   num_rows   N, 0 <= N < 2^32 - 1 (rows are packed into 32 bits), and
+ *              N * F <= 2^40 (else SEG_ERR_UNSUPPORTED).
  *   index      device, [N] int64, aligned to 8 bytes.  A row whose index is
  *              outside [0, dim_size) goes nowhere.
  *   dim_size   D >= 0 output rows; D == 0 returns SEG_OK and launches nothing.

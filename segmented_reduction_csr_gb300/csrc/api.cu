@@ -518,6 +518,8 @@ seg_status_t seg_scatter(const void* src, seg_dtype_t dtype, int64_t F, int64_t 
         reinterpret_cast<uintptr_t>(index) % 8 || reinterpret_cast<uintptr_t>(out_arg) % 8)
         return SEG_ERR_INVALID_ARGUMENT;
     if (ceil_div(dim_size * F, 8) > int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;
+    // one launch covers every element (no grid-stride loop): at most 2^30 CTAs
+    if (ceil_div(num_rows * F, int64_t(SC_NT) * SC_ITEMS) > (int64_t(1) << 30)) return SEG_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SEG_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);

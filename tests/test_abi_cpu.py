@@ -124,6 +124,7 @@ def test_scatter_host_checks_reject_before_any_cuda_call(lib):
     assert sc(64, 0, 1, 10, 64, 5, 3, 64, None, None) == 2          # mean on uint32
     assert sc(64, 2, 1, 10, 64, 5, 0, 64, 64, None) == 1            # arg with sum
     assert sc(64, 2, 1, 1 << 32, 64, 5, 2, 64, None, None) == 2     # rows do not fit 32 bits
+    assert sc(64, 2, 2048, (1 << 32) - 2, 64, 5, 0, 64, None, None) == 2   # N * F above 2^40: more than one launch
     assert sc(None, 2, 1, 10, 64, 5, 0, 64, None, None) == 1        # src NULL
     assert sc(64, 2, 1, 10, None, 5, 0, 64, None, None) == 1        # index NULL
     assert sc(64, 2, 1, 10, 64, 5, 0, None, None, None) == 1        # out NULL

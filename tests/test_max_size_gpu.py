@@ -1,5 +1,6 @@
 """Inputs past 2^31 elements on the GPU: the 64-bit index paths of the
-scalar kernel, the row kernel and the scan.
+scalar kernel, the row kernel, the scan, the offsets producers and the
+scatter path (atomic and sorted).
 
 At these sizes no CPU reference is run.  The values are ones with a few
 planted entries, so every expected result has a closed form that holds at
@@ -155,4 +156,57 @@ def test_scan_past_2_31_rows():
         a = OFFSETS[s]
         want = (r - a + 1) + sum(x - 1 for p, x in PLANTED.items() if a <= p <= r)
         assert g == want % (1 << 32), (r, g, want)
+    assert sr.device_status() == 0
+
+
+RUN_STARTS = [0, 5, 6, 1 << 20, (1 << 31) - 2, (1 << 31) - 1, 1 << 31, (1 << 31) + 1, (1 << 31) + 77, N - 1]
+
+
+def test_producers_past_2_31_elements():
+    import segmented_reduction_csr_gb300 as sr
+    _need_memory(4 * N + 4 * N + 4 * N + 8 * N)
+    keys = torch.empty(N, dtype=torch.int32, device="cuda")
+    bounds = RUN_STARTS + [N]
+    for k, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
+        keys[a:b] = 3 * k + 1          # consecutive runs differ
+    values, lengths, offsets = sr.rle(keys)
+    assert values.cpu().tolist() == [3 * k + 1 for k in range(len(RUN_STARTS))]
+    assert lengths.view(torch.int32).cpu().tolist() == [b - a for a, b in zip(bounds[:-1], bounds[1:])]
+    assert offsets.cpu().tolist() == bounds
+    del keys, values, lengths, offsets
+    torch.cuda.empty_cache()
+    flags = torch.zeros(N, dtype=torch.uint8, device="cuda")
+    flags[torch.tensor(RUN_STARTS[1:], dtype=torch.int64, device="cuda")] = 1
+    # index 0 is left unflagged: the offsets list the flagged indices only, then n
+    got = sr.flags_to_offsets(flags).cpu().tolist()
+    assert got == RUN_STARTS[1:] + [N]
+    assert sr.device_status() == 0
+
+
+def test_scatter_past_2_31_rows():
+    import segmented_reduction_csr_gb300 as sr
+    _need_memory(4 * N + 8 * N + 16 * N + 4 * N)
+    SH = 21
+    D = ((N - 1) >> SH) + 1
+    src = torch.ones(N, dtype=torch.float32, device="cuda")
+    planted = {3: -5.0, (1 << 31) + 100: 7.0, (1 << 31) + 101: 7.0, (1 << 31) - 9: 4.0}
+    for r, x in planted.items():
+        src[r] = x
+    index = torch.arange(N, dtype=torch.int64, device="cuda") >> SH
+    index[N - 1] = -1                  # goes nowhere
+    dst = [{r: x for r, x in planted.items() if (r >> SH) == d} for d in range(D)]
+    ranges = [(d << SH, min((d + 1) << SH, N - 1)) for d in range(D)]
+
+    def expect(op):
+        return [_segment_expect(a, b, dst[d], op) for d, (a, b) in enumerate(ranges)]
+
+    for det in (False, True):
+        s = sr.scatter(src, index, D, "sum", deterministic=det).double().cpu().numpy()
+        assert s.tolist() == [float(e[0]) for e in expect("sum")], det
+        torch.cuda.empty_cache()
+    for op in ("max", "min"):
+        o, arg = sr.scatter(src, index, D, op)
+        want = expect(op)
+        assert o.cpu().tolist() == [float(w[0]) for w in want], op
+        assert arg.cpu().tolist() == [w[1] for w in want], (op, "arg")
     assert sr.device_status() == 0
