@@ -81,9 +81,13 @@ def profile_traffic(config: str):
 
 class L2Flush:
     """Evict the inputs from L2 before a timed call: write a buffer of
-    2 x L2, then read another of 2 x L2, so that L2 holds clean lines that
-    belong to no input (the clean-cache state that ncu's cache control also
-    gives a profiled launch)."""
+    2 x L2, then read two others of 2 x L2 each, so that L2 holds clean lines
+    that belong to no input (the clean-cache state that ncu's cache control
+    also gives a profiled launch).  One read pass after the write is not
+    enough on GB300: the write's last dirty lines are still being written
+    back when the timed call starts, and that traffic lands in its time
+    (message-passing sum: 56.3 us after one read pass, 51.4 us after two,
+    51.5 us when nothing is written at all)."""
 
     def __init__(self, dev):
         import torch
@@ -91,12 +95,14 @@ class L2Flush:
         n = max(2 * l2, 256 << 20) // 4
         self.w = torch.empty(n, dtype=torch.float32, device=dev)
         self.r = torch.ones(n, dtype=torch.float32, device=dev)
+        self.r2 = torch.ones(n, dtype=torch.float32, device=dev)
         self.sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def __call__(self):
         import torch
         self.w.zero_()
         torch.sum(self.r, dim=0, out=self.sink)
+        torch.sum(self.r2, dim=0, out=self.sink)
 
 
 class ClockSampler:
@@ -284,7 +290,7 @@ def config_of(args, w):
       + ("; segmented scan (seg_scan), inclusive" if SCAN else ""),
         "segments": w.num_segments, "rows": w.num_rows, "features": w.feat,
         "cases": [f"{k}:{op}" for k, op in cases_of(w)],
-        "l2": "flushed before every timed call (a 2 x L2 write, then a 2 x L2 read: clean lines), outside the events"}
+        "l2": "flushed before every timed call (a 2 x L2 write, then two 2 x L2 reads: clean lines, write-backs drained), outside the events"}
 
 
 def run_ours(args, w: W.Workload):
@@ -495,7 +501,7 @@ def producer_config(args, w: W.Workload, n: int, runs: int):
     what = "segment-start flags (uint8)" if args.producer == "flags" else "ordered segment keys (uint32)"
     return {"workload": f"{args.producer} over the {what} of the {w.name} workload",
             "elements": n, "runs": runs, "producer": args.producer,
-            "l2": "flushed before every timed call (a 2 x L2 write, then a 2 x L2 read: clean lines), outside the events"}
+            "l2": "flushed before every timed call (a 2 x L2 write, then two 2 x L2 reads: clean lines, write-backs drained), outside the events"}
 
 
 def run_producer_reference(args, w: W.Workload):
@@ -654,7 +660,7 @@ def scatter_config(args, n, feat, dim):
     return {"workload": f"scatter {args.config}: {n:,} float32 rows x {feat} into {dim:,} outputs, "
                         "destinations uniform, unsorted (graph-reduce README 'Measured' shape)" + mode,
             "rows": n, "features": feat, "outputs": dim, "cases": [f"f32:{op}" for op in SCATTER_CASES],
-            "l2": "flushed before every timed call (a 2 x L2 write, then a 2 x L2 read: clean lines), outside the events"}
+            "l2": "flushed before every timed call (a 2 x L2 write, then two 2 x L2 reads: clean lines, write-backs drained), outside the events"}
 
 
 def run_scatter_reference(args):
