@@ -49,6 +49,10 @@ struct RowsSearchSmem {
 constexpr uint32_t RW_SMEM = ((sizeof(RowsSearchSmem) + 127) / 128) * 128;
 constexpr uint32_t RW_SMEM_STAGED = RW_NW * RW_NSR * RW_CB + RW_NW * RW_NSR * 8;
 static_assert(RW_SMEM <= RW_SMEM_STAGED && RW_SMEM_STAGED <= 227 * 1024, "staged rows fit one CTA per SM");
+// Offsets arrays up to this size are copied whole into a staged CTA's shared
+// memory (behind the search scratch) and searched there.
+constexpr uint32_t RW_SMALL_OFFS = 96 * 1024;
+static_assert(RW_SMEM + RW_SMALL_OFFS <= RW_SMEM_STAGED, "the offsets fit beside the search scratch");
 
 // VEC consecutive 32-bit elements, read once: no L1 allocation, L2 evict-first.
 template <int VEC>
@@ -173,17 +177,28 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     // End s sits at key(s) = (offsets[s+1] - o0) + RW_CW s; a cut at D takes
     // the I(D) = #{s : key(s) < D} ends before it and the rows before both
     // D - RW_CW I and the start of segment I.
+    // A small offsets array (staged shapes) is copied whole into shared
+    // memory and each boundary is a binary search there: no probe rounds.
     RowsSearchSmem* ss = reinterpret_cast<RowsSearchSmem*>(smem);
-    prefetch_offsets_slice(p.offsets, static_cast<uint64_t>(S + 1) * sizeof(OffT), cta, p.P, tid, RW_NTHREADS);
-    if (tid == 0) ss->o0 = clamp_off(__ldg(&offs[0]), N);
-    if (tid == 1) ss->oS = clamp_off(__ldg(&offs[S]), N);
-    for (int m = tid; m < RW_GRID; m += RW_NTHREADS) {
-        const int64_t sm = static_cast<int64_t>(m) * S / RW_GRID;
-        ss->graw[m] = clamp_off(__ldg(&offs[sm + 1]), N);
+    OffT* soffs = reinterpret_cast<OffT*>(smem + RW_SMEM);
+    const bool small = STAGED && static_cast<uint64_t>(S + 1) * sizeof(OffT) <= RW_SMALL_OFFS;
+    if (small) {
+        for (int64_t i = tid; i <= S; i += RW_NTHREADS) cp_async_small<sizeof(OffT)>(soffs + i, offs + i);
+        cp_async_commit();
+        cp_async_wait_all();
+    } else {
+        prefetch_offsets_slice(p.offsets, static_cast<uint64_t>(S + 1) * sizeof(OffT), cta, p.P, tid, RW_NTHREADS);
+        if (tid == 0) ss->o0 = clamp_off(__ldg(&offs[0]), N);
+        if (tid == 1) ss->oS = clamp_off(__ldg(&offs[S]), N);
+        for (int m = tid; m < RW_GRID; m += RW_NTHREADS) {
+            const int64_t sm = static_cast<int64_t>(m) * S / RW_GRID;
+            ss->graw[m] = clamp_off(__ldg(&offs[sm + 1]), N);
+        }
     }
     __syncthreads();
-    const int64_t o0 = ss->o0;
-    const int64_t oS = ss->oS < o0 ? o0 : ss->oS;
+    const int64_t o0 = small ? clamp_off(soffs[0], N) : ss->o0;
+    const int64_t oS_raw = small ? clamp_off(soffs[S], N) : ss->oS;
+    const int64_t oS = oS_raw < o0 ? o0 : oS_raw;
     const int64_t nrows = oS - o0;
     const int64_t total = nrows + RW_CW * S;
     const int64_t Wr = (total + NR - 1) / NR;
@@ -193,27 +208,39 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
         int64_t lo = D > nrows ? (D - nrows + RW_CW - 1) / RW_CW : 0;
         int64_t hi = (D + RW_CW - 1) / RW_CW;
         hi = hi < S ? hi : S;
-        int a = 0, b = RW_GRID;
-        while (a < b) {
-            const int mid = (a + b) >> 1;
-            const int64_t sm = static_cast<int64_t>(mid) * S / RW_GRID;
-            if (ss->graw[mid] - o0 + RW_CW * sm < D)
-                a = mid + 1;
-            else
-                b = mid;
+        if (small) {
+            // I = #{s : key(s) < D}: the first s in [lo, hi) with key(s) >= D
+            while (lo < hi) {
+                const int64_t mid = (lo + hi) >> 1;
+                if (clamp_off(soffs[mid + 1], N) - o0 + RW_CW * mid < D)
+                    lo = mid + 1;
+                else
+                    hi = mid;
+            }
+            hi = lo;
+        } else {
+            int a = 0, b = RW_GRID;
+            while (a < b) {
+                const int mid = (a + b) >> 1;
+                const int64_t sm = static_cast<int64_t>(mid) * S / RW_GRID;
+                if (ss->graw[mid] - o0 + RW_CW * sm < D)
+                    a = mid + 1;
+                else
+                    b = mid;
+            }
+            const int64_t lower = a > 0 ? static_cast<int64_t>(a - 1) * S / RW_GRID + 1 : 0;
+            const int64_t upper = a < RW_GRID ? static_cast<int64_t>(a) * S / RW_GRID : S;
+            lo = lo > lower ? lo : lower;
+            hi = hi < upper ? hi : upper;
+            if (hi < lo) hi = lo;
         }
-        const int64_t lower = a > 0 ? static_cast<int64_t>(a - 1) * S / RW_GRID + 1 : 0;
-        const int64_t upper = a < RW_GRID ? static_cast<int64_t>(a) * S / RW_GRID : S;
-        lo = lo > lower ? lo : lower;
-        hi = hi < upper ? hi : upper;
-        if (hi < lo) hi = lo;
         ss->D[tid] = D;
         ss->lo[tid] = lo;
         ss->hi[tid] = hi;
         ss->cnt[tid] = 0;
     }
     __syncthreads();
-    for (int round = 0; round < 64; ++round) {
+    for (int round = 0; round < (small ? 0 : 64); ++round) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int pidx = tid + u * RW_NTHREADS;
@@ -255,7 +282,7 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     }
     if (tid < nb) {
         const int64_t I = ss->lo[tid];
-        const int64_t oI = I > 0 ? clamp_off(__ldg(&offs[I]), N) - o0 : 0;
+        const int64_t oI = I > 0 ? clamp_off(small ? soffs[I] : __ldg(&offs[I]), N) - o0 : 0;
         int64_t R = ss->D[tid] - RW_CW * I;
         R = R < oI ? oI : R;
         R = R < 0 ? 0 : (R > nrows ? nrows : R);
@@ -271,6 +298,14 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     const int64_t Iu2 = ss->lo[bi + 1] > Iu ? ss->lo[bi + 1] : Iu;
     const int64_t Rc = ss->R[bi];                           // the cuts' rows
     const int64_t Rc2 = ss->R[bi + 1] > Rc ? ss->R[bi + 1] : Rc;
+    // the offsets of the segments that cross the cuts, while a shared copy lives
+    int64_t off_Iu = 0, off_Iu1 = 0, off_Iu2 = 0, off_Iu21 = 0;
+    if (small) {
+        off_Iu = clamp_off(soffs[Iu], N);
+        off_Iu1 = Iu < S ? clamp_off(soffs[Iu + 1], N) : 0;
+        off_Iu2 = Iu2 < S ? clamp_off(soffs[Iu2], N) : 0;
+        off_Iu21 = Iu2 < S ? clamp_off(soffs[Iu2 + 1], N) : 0;
+    }
     __syncthreads();   // the search scratch is dead from here on (staged rows reuse it)
     if (rg >= NR || Dlo >= Dhi) return;
     // Offsets of the segment that crosses each cut, and adoption: a segment
@@ -278,10 +313,12 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     // whole by the range that holds its end (which starts at the segment's
     // first row; the range before it stops there), so it needs no partial
     // and no ticket.  Both sides decide it from the same cut and offsets.
-    const int64_t off_Iu = clamp_off(__ldg(&offs[Iu]), N);
-    const int64_t off_Iu1 = Iu < S ? clamp_off(__ldg(&offs[Iu + 1]), N) : 0;
-    const int64_t off_Iu2 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2]), N) : 0;
-    const int64_t off_Iu21 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2 + 1]), N) : 0;
+    if (!small) {
+        off_Iu = clamp_off(__ldg(&offs[Iu]), N);
+        off_Iu1 = Iu < S ? clamp_off(__ldg(&offs[Iu + 1]), N) : 0;
+        off_Iu2 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2]), N) : 0;
+        off_Iu21 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2 + 1]), N) : 0;
+    }
     bool adopt_head = false, give_tail = false;
     if (Iu < Iu2 && off_Iu < Rc && Rc - off_Iu <= RW_ADOPT && rg > 0)
         adopt_head = (off_Iu - o0 + RW_CW * Iu) / Wr == rg - 1;
