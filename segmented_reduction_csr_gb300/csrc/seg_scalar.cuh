@@ -55,7 +55,7 @@ constexpr int SW_NSV = 2;                      // value stages per warp
 constexpr int SW_EMAXT = 160;                  // segment ends per tile
 constexpr int64_t SW_ADOPT = 1152;             // rows of a cut-crossing segment a unit adopts
 constexpr int SW_NDIAG = SW_NW + 1;            // unit boundaries per CTA
-constexpr int SW_GRID = 1024;                  // first-round probes, shared by all CTAs
+constexpr int SW_GRID = 512;                   // first-round probes, shared by all CTAs
 constexpr int SW_PROBES = 60;                  // later-round probes per boundary
 static_assert(SW_Q % 2 == 1, "conflict-free 128-bit row loads need SW_KR / 4 odd");
 constexpr int SW_PROBE_PASSES = (SW_NDIAG * SW_PROBES + SW_NTHREADS - 1) / SW_NTHREADS;   // per thread per round
