@@ -82,6 +82,11 @@ struct SearchSmem {
     int64_t o0, oS;
 };
 static_assert(sizeof(SearchSmem) <= SW_SMEM, "search scratch fits");
+// Offsets arrays up to this size are copied whole into shared memory (behind
+// the search scratch) and searched there.
+constexpr uint32_t SW_SEARCH_BYTES = ((sizeof(SearchSmem) + 127) / 128) * 128;
+constexpr uint32_t SW_SMALL_OFFS = 96 * 1024;
+static_assert(SW_SEARCH_BYTES + SW_SMALL_OFFS <= SW_SMEM, "the offsets fit beside the search scratch");
 
 // Last arriver of a multi-unit segment: partials tails[pc .. qc-1] then
 // heads[qc], combined by the whole warp: lane l folds a contiguous block in
@@ -149,17 +154,28 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     // before both D - SW_CW I and the start of segment I.  Round 1 reads a
     // fixed grid of SW_GRID keys that every CTA shares (so it hits L2); then
     // each boundary narrows its bracket with SW_PROBES probes per round.
+    // A small offsets array is copied whole into shared memory and each
+    // boundary is a binary search there: no probe rounds.
     SearchSmem* ss = reinterpret_cast<SearchSmem*>(smem);
-    prefetch_offsets_slice(p.offsets, static_cast<uint64_t>(S + 1) * OSZ, cta, p.P, tid, SW_NTHREADS);
-    if (tid == 0) ss->o0 = clamp_off(__ldg(&offs[0]), N);
-    if (tid == 1) ss->oS = clamp_off(__ldg(&offs[S]), N);
-    for (int m = tid; m < SW_GRID; m += SW_NTHREADS) {
-        const int64_t sm = static_cast<int64_t>(m) * S / SW_GRID;
-        ss->graw[m] = clamp_off(__ldg(&offs[sm + 1]), N);
+    OffT* soffs = reinterpret_cast<OffT*>(smem + SW_SEARCH_BYTES);
+    const bool small = static_cast<uint64_t>(S + 1) * OSZ <= SW_SMALL_OFFS;
+    if (small) {
+        for (int64_t i = tid; i <= S; i += SW_NTHREADS) cp_async_small<OSZ>(soffs + i, offs + i);
+        cp_async_commit();
+        cp_async_wait_all();
+    } else {
+        prefetch_offsets_slice(p.offsets, static_cast<uint64_t>(S + 1) * OSZ, cta, p.P, tid, SW_NTHREADS);
+        if (tid == 0) ss->o0 = clamp_off(__ldg(&offs[0]), N);
+        if (tid == 1) ss->oS = clamp_off(__ldg(&offs[S]), N);
+        for (int m = tid; m < SW_GRID; m += SW_NTHREADS) {
+            const int64_t sm = static_cast<int64_t>(m) * S / SW_GRID;
+            ss->graw[m] = clamp_off(__ldg(&offs[sm + 1]), N);
+        }
     }
     __syncthreads();
-    const int64_t o0 = ss->o0;
-    const int64_t oS = ss->oS < o0 ? o0 : ss->oS;
+    const int64_t o0 = small ? clamp_off(soffs[0], N) : ss->o0;
+    const int64_t oS_raw = small ? clamp_off(soffs[S], N) : ss->oS;
+    const int64_t oS = oS_raw < o0 ? o0 : oS_raw;
     const int64_t nrows = oS - o0;
     const int64_t total = nrows + SW_CW * S;
     const int64_t Wu = (total + U - 1) / U;
@@ -169,27 +185,39 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
         int64_t lo = D > nrows ? (D - nrows + SW_CW - 1) / SW_CW : 0;
         int64_t hi = (D + SW_CW - 1) / SW_CW;
         hi = hi < S ? hi : S;
-        int a = 0, b = SW_GRID;   // c = #{m : key(s_m) < D}
-        while (a < b) {
-            const int mid = (a + b) >> 1;
-            const int64_t sm = static_cast<int64_t>(mid) * S / SW_GRID;
-            if (ss->graw[mid] - o0 + SW_CW * sm < D)
-                a = mid + 1;
-            else
-                b = mid;
+        if (small) {
+            // I = #{s : key(s) < D}: the first s in [lo, hi) with key(s) >= D
+            while (lo < hi) {
+                const int64_t mid = (lo + hi) >> 1;
+                if (clamp_off(soffs[mid + 1], N) - o0 + SW_CW * mid < D)
+                    lo = mid + 1;
+                else
+                    hi = mid;
+            }
+            hi = lo;
+        } else {
+            int a = 0, b = SW_GRID;   // c = #{m : key(s_m) < D}
+            while (a < b) {
+                const int mid = (a + b) >> 1;
+                const int64_t sm = static_cast<int64_t>(mid) * S / SW_GRID;
+                if (ss->graw[mid] - o0 + SW_CW * sm < D)
+                    a = mid + 1;
+                else
+                    b = mid;
+            }
+            const int64_t lower = a > 0 ? static_cast<int64_t>(a - 1) * S / SW_GRID + 1 : 0;
+            const int64_t upper = a < SW_GRID ? static_cast<int64_t>(a) * S / SW_GRID : S;
+            lo = lo > lower ? lo : lower;
+            hi = hi < upper ? hi : upper;
+            if (hi < lo) hi = lo;
         }
-        const int64_t lower = a > 0 ? static_cast<int64_t>(a - 1) * S / SW_GRID + 1 : 0;
-        const int64_t upper = a < SW_GRID ? static_cast<int64_t>(a) * S / SW_GRID : S;
-        lo = lo > lower ? lo : lower;
-        hi = hi < upper ? hi : upper;
-        if (hi < lo) hi = lo;
         ss->D[tid] = D;
         ss->lo[tid] = lo;
         ss->hi[tid] = hi;
         ss->cnt[tid] = 0;
     }
     __syncthreads();
-    for (int round = 0; round < 64; ++round) {
+    for (int round = 0; round < (small ? 0 : 64); ++round) {
 #pragma unroll
         for (int u = 0; u < SW_PROBE_PASSES; ++u) {
             const int pidx = tid + u * SW_NTHREADS;
@@ -232,7 +260,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     if (tid < SW_NDIAG) {
         // rows before the cut: D - SW_CW I, but never fewer than segment I's start
         const int64_t I = ss->lo[tid];
-        const int64_t oI = I > 0 ? clamp_off(__ldg(&offs[I]), N) - o0 : 0;
+        const int64_t oI = I > 0 ? clamp_off(small ? soffs[I] : __ldg(&offs[I]), N) - o0 : 0;
         int64_t R = ss->D[tid] - SW_CW * I;
         R = R < oI ? oI : R;
         R = R < 0 ? 0 : (R > nrows ? nrows : R);
@@ -246,14 +274,23 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     const int64_t Iu2 = ss->lo[warp + 1] > Iu ? ss->lo[warp + 1] : Iu;
     const int64_t Rc = ss->R[warp];                              // the cuts' rows
     const int64_t Rc2 = ss->R[warp + 1] > Rc ? ss->R[warp + 1] : Rc;
+    // Offsets of the segment that crosses each cut (the head and tail logic
+    // needs them): from the shared copy while it lives, else loaded below.
+    int64_t off_Iu = 0, off_Iu1 = 0, off_Iu2 = 0, off_Iu21 = 0;
+    if (small) {
+        off_Iu = clamp_off(soffs[Iu], N);
+        off_Iu1 = Iu < S ? clamp_off(soffs[Iu + 1], N) : 0;
+        off_Iu2 = Iu2 < S ? clamp_off(soffs[Iu2], N) : 0;
+        off_Iu21 = Iu2 < S ? clamp_off(soffs[Iu2 + 1], N) : 0;
+    }
     __syncthreads();   // the search scratch is dead from here on
     if (Dlo >= Dhi) return;
-    // Offsets of the segment that crosses each cut (loaded now; the head and
-    // tail logic needs them).
-    const int64_t off_Iu = clamp_off(__ldg(&offs[Iu]), N);
-    const int64_t off_Iu1 = Iu < S ? clamp_off(__ldg(&offs[Iu + 1]), N) : 0;
-    const int64_t off_Iu2 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2]), N) : 0;
-    const int64_t off_Iu21 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2 + 1]), N) : 0;
+    if (!small) {
+        off_Iu = clamp_off(__ldg(&offs[Iu]), N);
+        off_Iu1 = Iu < S ? clamp_off(__ldg(&offs[Iu + 1]), N) : 0;
+        off_Iu2 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2]), N) : 0;
+        off_Iu21 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2 + 1]), N) : 0;
+    }
     // A segment that crosses just one cut, with at most SW_ADOPT rows before
     // it, is adopted whole by the unit that holds its end: that unit starts
     // at the segment's first row and the unit before it stops there, so no
