@@ -66,11 +66,16 @@ __device__ __forceinline__ unsigned long long start_bits(const RleParams& p, int
                                                          const Raw<FLAGS>& r) {
     unsigned long long bits = 0;
     if constexpr (FLAGS) {
+        // four flag bytes at a time: the high bit of each non-zero byte
+        // ((b & 0x7f) + 0x7f carries into bit 7 for b in 1..0x7f; b >= 0x80
+        // has it already), then one multiply gathers bits 7, 15, 23 and 31
+        // into bits 21..24 (the partial products never overlap)
 #pragma unroll
         for (int q = 0; q < RLE_FLAGS_PER / 4; ++q) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-                bits |= static_cast<unsigned long long>(((r.w[q] >> (8 * b)) & 0xffu) != 0) << (4 * q + b);
+            const uint32_t w = r.w[q];
+            const uint32_t hi = (((w & 0x7f7f7f7fu) + 0x7f7f7f7fu) | w) & 0x80808080u;
+            const uint32_t nib = ((hi >> 7) * 0x204081u) >> 21 & 0xfu;
+            bits |= static_cast<unsigned long long>(nib) << (4 * q);
         }
     } else {
         // the key before my first one: the previous lane's last key, or lane 0's load
