@@ -175,6 +175,46 @@ def test_uint32_offsets():
         _check(v, off, op, where=op)
 
 
+@pytest.mark.parametrize("feat", [1, 64, 100])
+def test_shared_memory_search_matches_probe_search(feat):
+    """Offsets arrays up to 96 KB are searched in shared memory, larger ones
+    by probe rounds (the scalar kernel and the staged row kernel; F = 100
+    takes the register-ring shape, which always probes).  With 20,000
+    segments, uint32 offsets (80 KB) take the first search and int64 offsets
+    (160 KB) the second.  For valid offsets both find the same partition, so
+    the results match bit for bit -- float sums included -- and both match
+    the oracle."""
+    rng = np.random.default_rng(20 + feat)
+    lengths = rng.integers(0, 2 * 48 // feat + 30, size=20_000)
+    lengths[rng.integers(0, lengths.size, 40)] = 0
+    off64 = W.offsets_from_lengths(lengths, np.int64)
+    off32 = off64.astype(np.uint32)
+    for kind in ("f32", "u32"):
+        v = _values(rng, int(off64[-1]), kind, feat)
+        dv = to_dev(v)
+        d64, d32 = to_dev(off64), to_dev(off32)
+        for op in _ops(kind):
+            g64, a64 = gpu_reduce(v, off64, op, dvals=dv, doffs=d64)
+            g32, a32 = gpu_reduce(v, off32, op, dvals=dv, doffs=d32)
+            assert np.array_equal(g64.view(np.uint32), g32.view(np.uint32)), (feat, kind, op)
+            if a64 is not None:
+                assert np.array_equal(a64, a32), (feat, kind, op, "arg")
+            assert_parity(v, off64, op, g64, a64, where=(feat, kind, op))
+
+
+@pytest.mark.parametrize("S", [12_287, 12_288])
+def test_shared_memory_search_threshold(S):
+    """int64 offsets of 12,287 segments (96 KB with the end) are searched in
+    shared memory, 12,288 by probe rounds: both sides of the boundary."""
+    rng = np.random.default_rng(S)
+    lengths = rng.integers(0, 40, size=S)
+    off = W.offsets_from_lengths(lengths, np.int64)
+    for feat in (1, 64):
+        v = _values(rng, int(off[-1]), "f32", feat)
+        for op in ("sum", "max"):
+            _check(v, off, op, where=(S, feat, op))
+
+
 def test_float_sums_are_bitwise_reproducible():
     import segmented_reduction_csr_gb300 as sr
     rng = np.random.default_rng(9)
