@@ -224,30 +224,129 @@ def step_bytes(w: W.Workload) -> int:
     return sum(case_bytes(w, k, op) for k, op in cases_of(w))
 
 
+# The reduction suite: the first workload is the headline (the largest one
+# that fits one GPU, 10M x 128 float32 rows in 100,000 power-law segments);
+# the others are timed in the same run and reported per config.
+SUITE = ("large", "mp", "skewed", "bulk", "tiny")
+CPU_CASE_BUDGET_S = 1.5      # sequential oracle seconds per case in one sample
+
+
+def _prefix_for(w: W.Workload, elements: float) -> int:
+    """Number of leading segments whose rows hold about `elements` values
+    (at least one segment)."""
+    off = w.offsets.astype(np.int64)
+    rows_needed = elements / max(1, w.feat)
+    s = int(np.searchsorted(off - off[0], rows_needed, side="left"))
+    return max(1, min(w.num_segments, s))
+
+
+def _calibrated_prefix(w: W.Workload, reduce, kind: str, op: str, budget_s: float) -> int:
+    """Leading segments that one sequential oracle call covers in about
+    budget_s: time a small prefix, scale by values per second."""
+    s_small = _prefix_for(w, 4e6)
+    sub = w.offsets[: s_small + 1]
+    t0 = time.perf_counter()
+    reduce(w.values[kind], sub, op)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    elems = max(1, (int(sub[-1]) - int(sub[0])) * w.feat + s_small)
+    return _prefix_for(w, elems / dt * budget_s)
+
+
+def _agrees(values, off, op, got, got_arg, exp, exp_arg) -> bool:
+    """The parity bar: integers, min / max values and args bit for bit;
+    float sums within 1e-5 * sum|x| + 1e-6 (means: over the length, plus one
+    rounding)."""
+    if op in ("min", "max") and not np.array_equal(got_arg, exp_arg):
+        return False
+    if values.dtype == np.float32 and op in ("sum", "mean"):
+        o = off.astype(np.int64)
+        a = np.abs(values[int(o[0]): int(o[-1])].astype(np.float64))
+        a = a.reshape(a.shape[0], -1)
+        cs = np.zeros((a.shape[0] + 1, a.shape[1]))
+        np.cumsum(a, axis=0, out=cs[1:])
+        tol = 1e-5 * (cs[o[1:] - o[0]] - cs[o[:-1] - o[0]]) + 1e-6
+        e64 = exp.astype(np.float64).reshape(tol.shape)
+        if op == "mean":
+            tol = tol / np.maximum(np.diff(o), 1)[:, None] + 2.0 ** -23 * np.abs(e64)
+        return bool((np.abs(got.astype(np.float64).reshape(tol.shape) - e64) <= tol).all())
+    return bool(np.array_equal(got.view(np.uint32), exp.view(np.uint32)))
+
+
+def cpu_leg(w: W.Workload, host_outs=None, budget_s: float = CPU_CASE_BUDGET_S):
+    """The CPU baseline: the oracle over a bounded prefix of the workload's
+    segments, every case, timed on one core (the sequential build) and on
+    all cores (the OpenMP build of the same loop).  When the GPU's outputs
+    are given, the oracle's outputs on that prefix are compared with them."""
+    import oracle
+    cases = cases_of(w)
+    seq = oracle.seg_reduce_sequential if SEQUENTIAL else oracle.seg_reduce
+    k0, op0 = cases[0]
+    s_take = _calibrated_prefix(w, seq, k0, op0, budget_s)
+    sub = w.offsets[: s_take + 1]
+    rows = int(sub[-1]) - int(sub[0])
+    nbytes = sum(W.algorithmic_bytes(rows, w.feat, s_take, w.offsets.dtype.itemsize, op) for _, op in cases)
+    t_seq = 0.0
+    checked, agree = 0, True
+    for k, op in cases:
+        t0 = time.perf_counter()
+        r = seq(w.values[k], sub, op)
+        t_seq += time.perf_counter() - t0
+        if host_outs is not None:
+            exp, exp_arg = r if isinstance(r, tuple) else (r, None)
+            got, got_arg = host_outs[(k, op)]
+            ok = _agrees(w.values[k], sub, op, got[:s_take], None if got_arg is None else got_arg[:s_take],
+                         exp, exp_arg)
+            agree = agree and ok
+            checked += 1
+    cores, t_par, par_note = 1, None, None
+    if not SEQUENTIAL:
+        try:
+            cores = oracle.parallel_threads()
+            t_par = 0.0
+            for k, op in cases:
+                t0 = time.perf_counter()
+                oracle.seg_reduce_parallel(w.values[k], sub, op)
+                t_par += time.perf_counter() - t0
+        except Exception as e:     # no OpenMP on this host: one core only
+            par_note = f"all-cores build unavailable: {e}"
+            cores, t_par = 1, None
+    sample = (f"first {s_take:,} of {w.num_segments:,} segments ({rows:,} rows), all {len(cases)} cases"
+              if s_take < w.num_segments else f"whole workload, all {len(cases)} cases")
+    one = {"value": nbytes / t_seq / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": sample, "seconds": t_seq}
+    if t_par is not None:
+        base = {"value": nbytes / t_par / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                "sample": sample, "seconds": t_par,
+                "build": "the oracle's loop with OpenMP over (segment, column) pairs", "one_core": one}
+    else:
+        base = dict(one)
+        if par_note:
+            base["note"] = par_note
+    parity = None
+    if host_outs is not None:
+        parity = {"oracle_prefix_segments": s_take, "cases": checked, "agree": agree}
+    return base, parity, s_take
+
+
 def run_reference(args, w: W.Workload):
-    """The oracle timed on the host cores over the same cases (a bounded sample
-    per step when the full workload would take too long)."""
+    """The reference arm: the oracle as it stands (the sequential C loop) on
+    one host core, each step every case over a bounded prefix of the
+    workload's segments."""
     import oracle
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
     cases = cases_of(w)
     offsets = w.offsets
-    # bound one step to about 2 s of CPU: prefix of segments
     if SCAN:
         def reduce(v, off, op):
             # the scan of the rows the prefix of offsets covers
             return oracle.seg_scan(v[: int(off[-1])], off, op)
     else:
         reduce = oracle.seg_reduce_sequential if SEQUENTIAL else oracle.seg_reduce
-    t0 = time.perf_counter()
-    for k, op in cases[:1]:
-        reduce(w.values[k], offsets, op)
-    one = time.perf_counter() - t0
-    est_step = one * len(cases)
-    frac = min(1.0, 2.0 / max(est_step, 1e-9))
+    k0, op0 = cases[0]
+    s_take = _calibrated_prefix(w, reduce, k0, op0, 2.0 / len(cases))
     S = w.num_segments
-    s_take = max(1, int(S * frac))
     sub = offsets[: s_take + 1]
     rows = int(sub[-1]) - int(sub[0])
     sample_bytes = sum((8 * int(sub[-1]) + sub.nbytes) if SCAN else
@@ -264,7 +363,7 @@ def run_reference(args, w: W.Workload):
         times.append(time.perf_counter() - t0)
     tot = sum(times)
     gbs = sample_bytes * args.steps / tot / 1e9
-    sample = (f"first {s_take} of {S} segments ({rows} rows), all {len(cases)} cases per step"
+    sample = (f"first {s_take:,} of {S:,} segments ({rows:,} rows), all {len(cases)} cases per step"
               if s_take < S else f"whole workload, all {len(cases)} cases per step")
     return {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "impl": "reference",
@@ -279,43 +378,64 @@ def run_reference(args, w: W.Workload):
     }
 
 
+WORKLOAD_TEXT = {
+    "tiny": "1,000 segments, ~7.5K rows, uint32 offsets",
+    "bulk": "1,000,000 segments, geometric lengths mean 16 (~16M rows), int64 offsets",
+    "mp": "1,000,000 rows x 64 float32 into 10,000 segments, int64 indptr",
+    "skewed": "64M float32 rows, 1M segments, Zipf(1.5) + 4 giants > 5M, 20% empty",
+    "large": "10M rows x 128 float32, 100,000 power-law segments, int64 indptr",
+    "large_1m": "1M rows x 128 float32, 10,000 power-law segments (a tenth of large, for profiling)",
+}
+
+
 def config_of(args, w):
-    return {"workload": f"{w.name}: " + {
-        "tiny": "1,000 segments, ~7.5K rows, uint32 offsets",
-        "bulk": "1,000,000 segments, geometric lengths mean 16 (~16M rows), int64 offsets",
-        "mp": "1,000,000 rows x 64 float32 into 10,000 segments, int64 indptr",
-        "skewed": "64M float32 rows, 1M segments, Zipf(1.5) + 4 giants > 5M, 20% empty",
-        "large": "10M rows x 128 float32, 100,000 power-law segments",
-    }[w.name] + ("; input-order float32 mode (seg_reduce_sequential)" if SEQUENTIAL else "")
-      + ("; segmented scan (seg_scan), inclusive" if SCAN else ""),
-        "segments": w.num_segments, "rows": w.num_rows, "features": w.feat,
-        "cases": [f"{k}:{op}" for k, op in cases_of(w)],
-        "l2": "flushed before every timed call (a 2 x L2 write, then two 2 x L2 reads: clean lines, write-backs drained), outside the events"}
+    return {"workload": f"{w.name}: " + WORKLOAD_TEXT[w.name]
+            + ("; input-order float32 mode (seg_reduce_sequential)" if SEQUENTIAL else "")
+            + ("; segmented scan (seg_scan), inclusive" if SCAN else ""),
+            "segments": w.num_segments, "rows": w.num_rows, "features": w.feat,
+            "cases": [f"{k}:{op}" for k, op in cases_of(w)],
+            "l2": "flushed before every timed call (a 2 x L2 write, then two 2 x L2 reads: clean lines, write-backs drained), outside the events"}
 
 
-def run_ours(args, w: W.Workload):
+def kernel_of(w: W.Workload) -> str:
+    if SCAN:
+        return "segred::rs_scan_kernel + rs_fix_kernel (with the bitmap launches)"
+    if SEQUENTIAL:
+        return "segred::seg_seq_kernel"
+    return "segred::seg_scalar_kernel" if w.feat == 1 else "segred::seg_rows2_kernel"
+
+
+def _to_dev(a, dev):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint32:
+        return torch.from_numpy(a.view(np.int32)).to(dev).view(torch.uint32)
+    return torch.from_numpy(a).to(dev)
+
+
+def _host(t):
+    import torch
+    if t is None:
+        return None
+    if t.dtype == torch.uint32:
+        return t.view(torch.int32).cpu().numpy().view(np.uint32)
+    return t.cpu().numpy()
+
+
+def measure_config(args, w: W.Workload, dev, world: int, flush, headline: bool):
+    """Everything about one workload on the GPU: upload, a 10-run bitwise
+    check of every case, warm-up, the timed steps (events per call, L2
+    flushed before each), then (headline only) the end-to-end step through
+    host buffers, and the CPU baseline with its oracle comparison."""
     import torch
 
     import segmented_reduction_csr_gb300 as sr
-    from segmented_reduction_csr_gb300 import build as srbuild
 
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    world, rank = dist_init("nccl", dev)
-    torch.cuda.set_device(dev)
-    srbuild.build()
-    lib = sr.load_library()
-
-    def to_dev(a):
-        a = np.ascontiguousarray(a)
-        if a.dtype == np.uint32:
-            return torch.from_numpy(a.view(np.int32)).to(dev).view(torch.uint32)
-        return torch.from_numpy(a).to(dev)
-
+    local = dev.index
     cases = cases_of(w)
-    dvals = {k: to_dev(v) for k, v in w.values.items()}
-    doff = to_dev(w.offsets)
+    stream = torch.cuda.current_stream(dev)
+    dvals = {k: _to_dev(v, dev) for k, v in w.values.items()}
+    doff = _to_dev(w.offsets, dev)
     outs = {}
     for k, op in cases:
         shape = (w.num_segments,) if w.feat == 1 else (w.num_segments, w.feat)
@@ -324,8 +444,6 @@ def run_ours(args, w: W.Workload):
         o = torch.empty(shape, dtype=dvals[k].dtype, device=dev)
         a = torch.empty(shape, dtype=torch.int64, device=dev) if (op in ("min", "max") and not SCAN) else None
         outs[(k, op)] = (o, a)
-    flush = L2Flush(dev)
-    stream = torch.cuda.current_stream(dev)
 
     def call(k, op):
         o, a = outs[(k, op)]
@@ -336,14 +454,31 @@ def run_ours(args, w: W.Workload):
         else:
             sr.seg_reduce(dvals[k], doff, op, out=o, out_arg=a, with_arg=a is not None)
 
+    # ---- ten runs of every case, bitwise identical to the first -----------------
+    repro = True
+    host_outs = {}
+    for k, op in cases:
+        call(k, op)
+        o, a = outs[(k, op)]
+        first = (o.clone(), a.clone() if a is not None else None)
+        for _ in range(9):
+            call(k, op)
+            same = torch.equal(o.view(torch.int32), first[0].view(torch.int32))
+            if a is not None:
+                same = same and torch.equal(a, first[1])
+            repro = repro and bool(same)
+        host_outs[(k, op)] = (_host(first[0]), _host(first[1]))
+        del first
+    torch.cuda.synchronize(dev)
+    assert sr.device_status(stream) == 0
+
     for _ in range(args.warmup):
         for k, op in cases:
             flush()
             call(k, op)
     torch.cuda.synchronize(dev)
-    assert sr.device_status(stream) == 0
 
-    # ---- device-resident timing --------------------------------------------
+    # ---- device-resident timing --------------------------------------------------
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps * len(cases))]
     clocks = ClockSampler(local)
@@ -366,8 +501,8 @@ def run_ours(args, w: W.Workload):
     per_call = [s.elapsed_time(e) for s, e in ev]             # ms
     kernel_ms = max_over_ranks(sum(per_call), world, dev)
     assert sr.device_status(stream) == 0
+    peak, _ = measured_peak()
     bytes_step = step_bytes(w)
-    value = whole_job_gbs(world, bytes_step, args.steps, kernel_ms)
     by_case = {}
     for idx, (k, op) in enumerate(cases * args.steps):
         by_case.setdefault((k, op), []).append(per_call[idx])
@@ -375,10 +510,33 @@ def run_ours(args, w: W.Workload):
     for k, op in cases:
         ms = statistics.median(by_case[(k, op)])
         b = case_bytes(w, k, op)
-        breakdown.append({"case": f"{k}:{op}", "us_median": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
-                          "bytes": b})
+        breakdown.append({"config": w.name, "case": f"{k}:{op}", "us_median": ms * 1e3,
+                          "gbs": b / (ms * 1e-3) / 1e9, "pct_of_peak": 100.0 * b / (ms * 1e-3) / 1e9 / peak,
+                          "segments_per_s": w.num_segments / (ms * 1e-3), "bytes": b})
+    res = {"w": w, "per_call": per_call, "kernel_ms": kernel_ms, "clocks": clk, "wall": wall,
+           "breakdown": breakdown, "bytes_step": bytes_step, "reproducible": repro,
+           "value": whole_job_gbs(world, bytes_step, args.steps, kernel_ms)}
 
-    # ---- end to end through host buffers ------------------------------------
+    if headline:
+        res["e2e"] = _e2e(args, w, dev, world, stream, dvals, doff, outs, call, bytes_step)
+    if world == 1 and not args.no_cpu_baseline and not SCAN:
+        base, parity, _ = cpu_leg(w, host_outs, CPU_CASE_BUDGET_S if headline else 0.5)
+        res["cpu_baseline"] = base
+        res["parity"] = parity
+    del dvals, doff, outs
+    torch.cuda.empty_cache()
+    return res
+
+
+def _e2e(args, w, dev, world, stream, dvals, doff, outs, call, bytes_step):
+    """The same bytes through host buffers: every step copies its inputs up
+    from pinned memory, runs the calls and copies every output back.  The
+    step is pipelined over three streams: the offsets and then each dtype's
+    values go up on a copy stream; a dtype's calls start on the compute
+    stream as soon as its values have arrived; its outputs go back on a
+    third stream while the next dtype computes."""
+    import torch
+    cases = cases_of(w)
     host_vals = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int32) if v.dtype == np.uint32 else v)).pin_memory()
                  for k, v in w.values.items()}
     host_off = torch.from_numpy(w.offsets).pin_memory()
@@ -388,12 +546,6 @@ def run_ours(args, w: W.Workload):
     h2d = sum(t.numel() * t.element_size() for t in host_vals.values()) + host_off.numel() * host_off.element_size()
     d2h = sum(o.numel() * o.element_size() + (a.numel() * 8 if a is not None else 0)
               for o, a in host_outs.values())
-
-    # The step is pipelined over three streams: the offsets and then each
-    # dtype's values go up on a copy stream; a dtype's calls start on the
-    # compute stream as soon as its values have arrived; its outputs go back
-    # on a third stream while the next dtype computes.  The step ends when
-    # every output is on the host.
     up = torch.cuda.Stream(dev)
     down = torch.cuda.Stream(dev)
     kinds = list(dict.fromkeys(k for k, _ in cases))
@@ -436,44 +588,73 @@ def run_ours(args, w: W.Workload):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    e2e_val = whole_job_gbs(world, bytes_step, args.steps, e2e_ms)
+    return {"value": whole_job_gbs(world, bytes_step, args.steps, e2e_ms), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipelined": "each dtype's values go up while the previous dtype computes; its outputs come back while the next computes"}
 
-    # ---- CPU baseline (rank 0, N == 1 only) --------------------------------
-    cpu = None
-    if world == 1 and not args.no_cpu_baseline:
-        ref = run_reference(argparse.Namespace(steps=1, warmup=0, gpus=1), w)
-        cpu = ref["cpu_baseline"]
 
+def run_ours(args, names):
+    import torch
+
+    import segmented_reduction_csr_gb300 as sr
+    from segmented_reduction_csr_gb300 import build as srbuild
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    world, rank = dist_init("nccl", dev)
+    torch.cuda.set_device(dev)
+    srbuild.build()
+    sr.load_library()
+    flush = L2Flush(dev)
     peak, peak_kind = measured_peak()
-    achieved = bytes_step * args.steps / (sum(per_call) * 1e-3) / 1e9
+    results = [measure_config(args, W.make(name), dev, world, flush, headline=(i == 0))
+               for i, name in enumerate(names)]
+    head = results[0]
+    w = head["w"]
+    cases = cases_of(w)
+    achieved = head["bytes_step"] * args.steps / (sum(head["per_call"]) * 1e-3) / 1e9
     traffic = None if (SEQUENTIAL or SCAN) else profile_traffic(w.name)
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": kernel_ms / args.steps, "higher_is_better": True,
+        "ms_per_step": head["kernel_ms"] / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "u32/s32/f32" if (w.feat == 1 and not SEQUENTIAL) else "f32", "data": "synthetic",
         "config": config_of(args, w),
-        "pct_of_peak": 100.0 * value / world / peak, "peak_gbs": peak, "peak_kind": peak_kind,
-        "pct_of_8tbs": 100.0 * value / world / 8000.0,
-        "segments_per_s": world * w.num_segments * len(cases) * args.steps / (kernel_ms * 1e-3),
+        "pct_of_peak": 100.0 * head["value"] / world / peak, "peak_gbs": peak, "peak_kind": peak_kind,
+        "pct_of_8tbs": 100.0 * head["value"] / world / 8000.0,
+        "segments_per_s": world * w.num_segments * len(cases) * args.steps / (head["kernel_ms"] * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": ("segred::rs_scan_kernel + rs_fix_kernel (with the bitmap launches)" if SCAN else
-                                "segred::seg_seq_kernel" if SEQUENTIAL else
-                                ("segred::seg_scalar_kernel" if w.feat == 1 else "segred::seg_rows2_kernel"))
-                               + " (every launch of the step)",
-                     "peak_note": f"{peak_kind} HBM copy bandwidth"},
-        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "pipelined": "each dtype's values go up while the previous dtype computes; its outputs come back while the next computes",
-                "d2h_bytes_per_step": d2h},
+                     "kernel": kernel_of(w) + " (every launch of the step)",
+                     "peak_note": f"{peak_kind} HBM copy bandwidth",
+                     "traffic_note": ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
+                                      "averaged over the step's cases" +
+                                      ("; taken on the 1M x 128 case and scaled by rows to the full launch"
+                                       if w.name == "large" else ""))},
+        "e2e": head["e2e"],
         "gpu_launches": args.steps * len(cases),
-        "clocks": clk,
-        "wall_s_timed_region": wall,
-        "breakdown": breakdown,
+        "clocks": head["clocks"],
+        "wall_s_timed_region": head["wall"],
+        "reproducible_10_runs": head["reproducible"],
+        "breakdown": [b for r in results for b in r["breakdown"]],
+        "configs": [{"workload": config_of(args, r["w"])["workload"],
+                     "value": r["value"], "unit": "GB/s",
+                     "pct_of_peak": 100.0 * r["value"] / world / peak,
+                     "ms_per_step": r["kernel_ms"] / args.steps,
+                     "segments_per_s": world * r["w"].num_segments * len(cases_of(r["w"])) * args.steps
+                     / (r["kernel_ms"] * 1e-3),
+                     "kernel": kernel_of(r["w"]),
+                     "cases": [f"{k}:{op}" for k, op in cases_of(r["w"])],
+                     "reproducible_10_runs": r["reproducible"],
+                     "oracle_check": r.get("parity"),
+                     "clocks": r["clocks"]} for r in results],
     }
-    if cpu is not None:
-        line["cpu_baseline"] = cpu
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if head.get("parity") is not None:
+        line["oracle_check"] = head["parity"]
     if world > 1:
         torch.distributed.destroy_process_group()
     return line if rank == 0 else None
@@ -806,7 +987,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="bulk", choices=W.NAMES + ("mp16",))
+    ap.add_argument("--config", default=None, choices=W.NAMES + ("mp16", "large_1m"),
+                    help="one workload only (default: the suite, large first)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--producer", default=None, choices=["rle", "unique", "flags"])
@@ -825,6 +1007,7 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.scatter:
+        args.config = args.config or "mp"
         if args.config not in ("mp", "mp16"):
             ap.error("--scatter runs on the mp or mp16 shape")
         line = run_scatter_reference(args) if args.impl == "reference" else run_scatter_ours(args)
@@ -832,6 +1015,7 @@ def main():
             print(json.dumps(line), flush=True)
         return
     if args.producer is not None:
+        args.config = args.config or "bulk"
         if args.config not in ("bulk", "skewed"):
             ap.error("--producer runs on the bulk or skewed workload")
         w = W.make(args.config, with_values=False)
@@ -839,11 +1023,18 @@ def main():
         if line is not None:
             print(json.dumps(line), flush=True)
         return
-    w = W.make(args.config)
-    if args.impl == "reference":
-        line = run_reference(args, w)
+    if args.config is not None:
+        names = (args.config,)
+    elif SCAN or SEQUENTIAL:
+        names = ("bulk",)
     else:
-        line = run_ours(args, w)
+        names = SUITE
+    if args.config == "mp16":
+        ap.error("mp16 is a scatter shape")
+    if args.impl == "reference":
+        line = run_reference(args, W.make(names[0]))
+    else:
+        line = run_ours(args, names)
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -167,11 +167,12 @@ seg_status_t seg_reduce_plan(seg_dtype_t dtype, int64_t F, int64_t num_values,
  * bytes for F == 1; 2 * grid * 8 * 32 * vec * (4, or 12 for min / max)
  * bytes for F > 1, grid and vec being seg_reduce_plan's).  On a 152-SM GPU
  * every F == 1 call, every sum and mean, and min / max on rows loaded at
- * most two columns at a time fit; min / max on rows loaded four columns at
- * a time (F >= 128, F % 4 == 0, 16-byte aligned rows) fit while the grid is
- * at most 84 CTAs (seg_reduce_plan reports workspace_bytes).  A call that
- * would need more returns SEG_ERR_SCRATCH_LIMIT before launching anything;
- * use seg_reduce for it.
+ * most two columns at a time fit.  The planner loads four columns at a time
+ * whenever F > 64, F % 4 == 0 and the rows are 16-byte aligned; min / max on
+ * such rows need 24 KiB per CTA and fit while the grid is at most 84 CTAs
+ * (for F = 96, up to about 86,000 weighted rows; seg_reduce_plan reports
+ * workspace_bytes).  A call that would need more returns
+ * SEG_ERR_SCRATCH_LIMIT before launching anything; use seg_reduce for it.
  *
  * Set-up.  The first call on each device looks up the array's address
  * (cudaGetSymbolAddress, with that device current), clears its ticket words

@@ -9,6 +9,9 @@ Two independent implementations live here:
 * ``seg_reduce``: the sequential C loop in ``seg_oracle.c`` (built with gcc,
   called through ctypes) -- the oracle proper, fast enough for the full
   synthetic workloads.
+* ``seg_reduce_parallel``: the same C loop built a second time with OpenMP
+  over (segment, column) pairs, for the benchmark's all-cores CPU baseline
+  only (each output is computed exactly as in the sequential build).
 * ``brute.seg_reduce``: a pure-Python restatement with Python integers and
   ``math.fsum`` for tiny inputs, used to pin the C oracle.
 * ``seg_reduce_sequential``: the input-order float32 sum / mean of
@@ -52,6 +55,7 @@ _SCAN_SRC = os.path.join(_HERE, "scan_oracle.c")
 _SCAN_LIB = os.path.join(_LIBDIR, "libsegscanoracle.so")
 _SEQ_SRC = os.path.join(_HERE, "seq_oracle.c")
 _SEQ_LIB = os.path.join(_LIBDIR, "libsegseqoracle.so")
+_PAR_LIB = os.path.join(_LIBDIR, "libsegoracle_par.so")
 
 # Codes private to seg_oracle.c.
 _DT = {np.dtype(np.uint32): 0, np.dtype(np.int32): 1, np.dtype(np.float32): 2}
@@ -64,11 +68,11 @@ _lock = threading.Lock()
 _lib = None
 
 
-def compile_source(src: str, dst: str) -> str:
+def compile_source(src: str, dst: str, extra=()) -> str:
     """gcc -O2 without fast-math or FMA contraction, as a shared library."""
     tmp = dst + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
-           "-ffp-contract=off", "-o", tmp, src]
+           "-ffp-contract=off", *extra, "-o", tmp, src]
     subprocess.run(cmd, check=True)
     os.replace(tmp, dst)
     return dst
@@ -96,7 +100,35 @@ def load_library(path: str):
         ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_threads.restype = ctypes.c_int
+    lib.oracle_threads.argtypes = []
     return lib
+
+
+_par_lib = None
+
+
+def load_parallel_library():
+    """The all-cores build of seg_oracle.c (OpenMP over (segment, column)
+    pairs), compiled on first use; raises if gcc has no OpenMP."""
+    global _par_lib
+    with _lock:
+        if _par_lib is None:
+            os.makedirs(_LIBDIR, exist_ok=True)
+            if not os.path.exists(_PAR_LIB) or os.path.getmtime(_PAR_LIB) < os.path.getmtime(_SRC):
+                compile_source(_SRC, _PAR_LIB, ("-fopenmp", "-DORC_PARALLEL_SEGMENTS"))
+            _par_lib = load_library(_PAR_LIB)
+    return _par_lib
+
+
+def parallel_threads() -> int:
+    """Threads the all-cores build runs on (OMP_NUM_THREADS, else every core)."""
+    return int(load_parallel_library().oracle_threads())
+
+
+def seg_reduce_parallel(values, offsets, op: str, with_arg: bool = True):
+    """``seg_reduce`` through the all-cores build: the same outputs, bit for bit."""
+    return seg_reduce(values, offsets, op, with_arg=with_arg, lib=load_parallel_library())
 
 
 def _load():

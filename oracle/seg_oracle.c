@@ -34,9 +34,19 @@
  *   - mean is defined for float32 only.
  *
  * No blocking, no reordering, no parallelism: one sequential loop.
+ *
+ * The CPU baseline of the benchmark also times this same loop on all host
+ * cores: compiled a second time with ORC_PARALLEL_SEGMENTS and -fopenmp, the
+ * (segment, column) iterations, which write disjoint outputs and each run
+ * the same sequential inner loop, are shared among threads.  Each output is
+ * then computed exactly as in the sequential build.  The parity checks use
+ * the sequential build only.
  */
 #include <stdint.h>
 #include <string.h>
+#ifdef ORC_PARALLEL_SEGMENTS
+#include <omp.h>
+#endif
 
 /* Codes private to this file (the Python wrapper passes them). */
 #define ORC_DT_U32 0
@@ -182,10 +192,13 @@ int oracle_seg_reduce(const void *values, int dtype, int64_t F,
     }
 
     int with_arg = (op == ORC_MIN || op == ORC_MAX) && out_arg != 0;
+#ifdef ORC_PARALLEL_SEGMENTS
+#pragma omp parallel for collapse(2) schedule(dynamic, 64)
+#endif
     for (int64_t s = 0; s < S; ++s) {
-        int64_t b = offset_at(offsets, off_dtype, s);
-        int64_t e = offset_at(offsets, off_dtype, s + 1);
         for (int64_t f = 0; f < F; ++f) {
+            int64_t b = offset_at(offsets, off_dtype, s);
+            int64_t e = offset_at(offsets, off_dtype, s + 1);
             int64_t o = s * F + f;
             int64_t arg = -1;
             if (e == b) {
@@ -209,4 +222,14 @@ int oracle_seg_reduce(const void *values, int dtype, int64_t F,
         }
     }
     return ORC_OK;
+}
+
+/* Threads the loop above runs on: 1 in the sequential build. */
+int oracle_threads(void)
+{
+#ifdef ORC_PARALLEL_SEGMENTS
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
 }

@@ -46,13 +46,29 @@ def gpu_reduce(values: np.ndarray, offsets: np.ndarray, op: str, dvals=None, dof
 
 
 def abs_sums(values: np.ndarray, offsets: np.ndarray) -> np.ndarray:
-    """sum(|x|) per segment (and column), in float64."""
-    v = np.abs(values.astype(np.float64))
-    v2 = v.reshape(v.shape[0], int(np.prod(v.shape[1:], dtype=np.int64)))
-    cs = np.zeros((v2.shape[0] + 1, v2.shape[1]), dtype=np.float64)
-    np.cumsum(v2, axis=0, out=cs[1:])
+    """sum(|x|) per segment (and column), in float64, from a running prefix
+    built block by block (a few hundred MB at a time, whatever the input
+    size).  Offsets must be nondecreasing."""
+    feat = int(np.prod(values.shape[1:], dtype=np.int64))
+    v2 = values.reshape(values.shape[0], feat)
+    n = v2.shape[0]
     off = offsets.astype(np.int64)
-    r = cs[off[1:]] - cs[off[:-1]]
+    pre = np.empty((off.shape[0], feat), dtype=np.float64)   # prefix at each offset
+    carry = np.zeros(feat, dtype=np.float64)
+    block = max(1, (1 << 24) // feat)
+    lo = 0
+    for r0 in range(0, n, block):
+        r1 = min(n, r0 + block)
+        cs = np.empty((r1 - r0 + 1, feat), dtype=np.float64)
+        cs[0] = carry
+        np.cumsum(np.abs(v2[r0:r1].astype(np.float64)), axis=0, out=cs[1:])
+        cs[1:] += carry
+        hi = int(np.searchsorted(off, r1, side="left"))
+        pre[lo:hi] = cs[off[lo:hi] - r0]
+        lo = hi
+        carry = cs[-1]
+    pre[lo:] = carry
+    r = pre[1:] - pre[:-1]
     return r.reshape((offsets.shape[0] - 1,) + values.shape[1:])
 
 

@@ -73,3 +73,43 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["n_gpus"] == 2
+
+
+def test_cpu_leg_compares_the_oracle_prefix_with_given_outputs():
+    """The CPU-baseline leg times the oracle over a prefix of the segments and
+    checks the outputs it is given on that prefix: outputs equal to the
+    oracle's agree, one planted difference does not."""
+    pytest.importorskip("torch")
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import oracle
+    import workloads as W
+    w = W.make("tiny")
+    outs = {}
+    for k, op in w.cases:
+        r = oracle.seg_reduce(w.values[k], w.offsets, op)
+        outs[(k, op)] = r if isinstance(r, tuple) else (r, None)
+    base, parity, s_take = bench.cpu_leg(w, outs, budget_s=0.05)
+    assert parity["agree"] and parity["cases"] == len(w.cases) and s_take >= 1
+    assert base["kind"] == "oracle" and base["value"] > 0 and base["cores"] >= 1
+    bad = dict(outs)
+    o, a = bad[("f32", "max")]
+    a = a.copy()
+    a[0] = a[0] + 1 if a[0] >= 0 else 0
+    bad[("f32", "max")] = (o, a)
+    assert not bench.cpu_leg(w, bad, budget_s=0.05)[1]["agree"]
+    # float sums: within the bar agrees, far outside it does not
+    o = outs[("f32", "sum")][0].copy()
+    o[np.argmax(np.abs(o))] += 1.0
+    bad2 = dict(outs)
+    bad2[("f32", "sum")] = (o, None)
+    assert not bench.cpu_leg(w, bad2, budget_s=0.05)[1]["agree"]
+
+
+def test_suite_headline_is_the_largest_workload():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.SUITE[0] == "large"
+    assert set(bench.SUITE) == {"tiny", "bulk", "mp", "skewed", "large"}

@@ -67,3 +67,34 @@ def test_oracle_agrees_with_torch_segment_reduce():
             assert np.array_equal(got, ref)
         else:
             np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-6)
+
+
+def test_all_cores_build_equals_sequential_build():
+    """The benchmark's all-cores CPU baseline times the same C loop built with
+    OpenMP over (segment, column) pairs; every output must be bit for bit
+    the sequential build's (each pair runs the same sequential inner loop)."""
+    try:
+        oracle.load_parallel_library()
+    except Exception as e:   # no OpenMP in this gcc: the baseline reports one core
+        pytest.skip(f"no OpenMP build: {e}")
+    rng = np.random.default_rng(23)
+    lengths = rng.integers(0, 60, size=5000)
+    lengths[::11] = 0
+    lengths[7] = 40_000
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    n = int(off[-1])
+    for feat in (1, 5):
+        shape = (n,) if feat == 1 else (n, feat)
+        cases = {"f32": rng.standard_normal(shape).astype(np.float32),
+                 "s32": rng.integers(-2**31, 2**31, size=shape).astype(np.int32)}
+        cases["u32"] = cases["s32"].view(np.uint32)
+        for kind, v in cases.items():
+            for op in ("sum", "min", "max") + (("mean",) if kind == "f32" else ()):
+                a = oracle.seg_reduce(v, off, op)
+                b = oracle.seg_reduce_parallel(v, off, op)
+                if isinstance(a, tuple):
+                    assert np.array_equal(a[0].view(np.uint32), b[0].view(np.uint32)), (feat, kind, op)
+                    assert np.array_equal(a[1], b[1]), (feat, kind, op)
+                else:
+                    assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (feat, kind, op)
+    assert oracle.parallel_threads() >= 1

@@ -26,6 +26,10 @@ large      10,000,000 rows x 128 float32 N(0, 1) over 100,000 segments with
            to 10M rows, each >= 1); int64.
 =========  ===================================================================
 
+``large_1m`` is the large recipe at a tenth of the size (1,000,000 rows x
+128 over 10,000 segments, seed ``20261202 + 50``): a case small enough for
+hardware-counter captures of the large workload's kernel shape.
+
 The mp workload draws i.i.d. rows directly in destination order: permuting
 i.i.d. rows by a stable sort of their destinations gives the same
 distribution, so the sort is not materialised.
@@ -136,8 +140,8 @@ def _fill_values(shape, seed: int, kind: str, lo=None, hi=None) -> np.ndarray:
 def make(name: str, with_values: bool = True) -> Workload:
     """Draw workload ``name``; ``with_values=False`` draws only the offsets
     (the values then hold zero-row placeholders of the right dtype)."""
-    idx = NAMES.index(name)
-    seed = SEED_BASE + idx
+    idx = NAMES.index(name) if name in NAMES else None
+    seed = SEED_BASE + (idx if idx is not None else 50)
     rng = np.random.Generator(np.random.PCG64(seed))
 
     def _fill(shape, sd, kind, lo=None, hi=None):
@@ -189,9 +193,9 @@ def make(name: str, with_values: bool = True) -> Workload:
         vals = {"f32": _fill((N,), seed + 1000, "normal")}
         return Workload(name, off, vals, 1, tuple(("f32", op) for op in
                                                   ("sum", "min", "max")), seed)
-    if name == "large":
-        N, F, S = 10_000_000, 128, 100_000
-        draws = np.minimum(np.floor(rng.pareto(1.1, size=S) + 1.0), 10_000_000)
+    if name in ("large", "large_1m"):
+        N, F, S = (10_000_000, 128, 100_000) if name == "large" else (1_000_000, 128, 10_000)
+        draws = np.minimum(np.floor(rng.pareto(1.1, size=S) + 1.0), N)
         off = offsets_from_lengths(scale_to_total(draws, N))
         vals = {"f32": _fill((N, F), seed + 1000, "normal")}
         return Workload(name, off, vals, F, (("f32", "sum"), ("f32", "max")), seed)
