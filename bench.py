@@ -43,7 +43,7 @@ import workloads as W  # noqa: E402
 METRIC = "segmented-reduce effective HBM GB/s and % of GB300 peak; segments/s (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
 # what shapes the reduction's launches: its kernels and its host planner
-KERNEL_SOURCES = ["ptx.cuh", "seg_common.cuh", "seg_rows2.cuh", "seg_scalar.cuh", "seg_pick.cuh",
+KERNEL_SOURCES = ["ptx.cuh", "seg_common.cuh", "seg_rows2.cuh", "seg_scalar.cuh", "seg_small.cuh", "seg_pick.cuh",
                   "seg_plan.cuh", "seg_f32.cu", "seg_u32.cu", "seg_s32.cu"]
 
 

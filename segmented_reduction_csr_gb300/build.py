@@ -19,7 +19,7 @@ LIBDIR = os.path.join(HERE, "lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "libsegreduce.so")
 UNITS = ["seg_f32.cu", "seg_u32.cu", "seg_s32.cu", "seg_rle.cu", "seg_seq.cu", "seg_scatter.cu", "seg_scan.cu", "seg_sort.cu", "api.cu"]
-HEADERS = ["ptx.cuh", "seg_common.cuh", "seg_rows2.cuh", "seg_scalar.cuh", "seg_pick.cuh", "seg_rle.cuh", "seg_seq.cuh", "seg_scatter.cuh", "seg_scan.cuh", "seg_plan.cuh", "seg_sort.cuh"]
+HEADERS = ["ptx.cuh", "seg_common.cuh", "seg_rows2.cuh", "seg_scalar.cuh", "seg_small.cuh", "seg_pick.cuh", "seg_rle.cuh", "seg_seq.cuh", "seg_scatter.cuh", "seg_scan.cuh", "seg_plan.cuh", "seg_sort.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr"]

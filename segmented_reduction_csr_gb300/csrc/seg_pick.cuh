@@ -5,6 +5,7 @@
 #pragma once
 #include "seg_rows2.cuh"
 #include "seg_scalar.cuh"
+#include "seg_small.cuh"
 
 namespace segred {
 
@@ -17,7 +18,8 @@ enum : int {
     SHAPE_STAGED_VEC1 = 5,  // 1 < F <= 32, F % 4 == 0, 16-byte aligned: rows staged by bulk copies
     SHAPE_STAGED_VEC2 = 6,  // 32 < F <= 64, same
     SHAPE_STAGED_VEC4 = 7,  // 64 < F <= 128, same
-    SHAPE_COUNT = 8
+    SHAPE_SMALL = 8,        // F == 1, at most SM_MAXR rows and SM_MAXS segments: one CTA
+    SHAPE_COUNT = 9
 };
 
 template <class T, int OP, class OffT>
@@ -30,6 +32,7 @@ const void* pick_shape(int shape) {
         case SHAPE_STAGED_VEC1: return reinterpret_cast<const void*>(&seg_rows2_kernel<T, OP, OffT, 1, true>);
         case SHAPE_STAGED_VEC2: return reinterpret_cast<const void*>(&seg_rows2_kernel<T, OP, OffT, 2, true>);
         case SHAPE_STAGED_VEC4: return reinterpret_cast<const void*>(&seg_rows2_kernel<T, OP, OffT, 4, true>);
+        case SHAPE_SMALL: return reinterpret_cast<const void*>(&seg_small_kernel<T, OP, OffT>);
         default: return nullptr;
     }
 }

@@ -40,6 +40,20 @@ seg_status_t plan_launch(seg_dtype_t dtype, int64_t F, int64_t num_values,
     if (offsets_dtype == SEG_OFF_U32 && num_values > int64_t(UINT32_MAX)) return SEG_ERR_INVALID_ARGUMENT;
 
     std::memset(pl, 0, sizeof(*pl));
+    if (F == 1 && num_values <= SM_MAXR && S <= SM_MAXS) {
+        // a small input: one CTA, bound by latency (no partition, no scratch use)
+        pl->grid = 1;
+        pl->block = SM_NT;
+        pl->slot_threads = 1;
+        pl->items_per_slot = 32;
+        pl->vec = 1;
+        pl->vecs_per_thread = 1;
+        pl->max_ends = static_cast<int32_t>(S);
+        pl->kernel_variant = SHAPE_SMALL;
+        pl->smem_bytes = SM_SMEM;
+        pl->workspace_bytes = ticket_region_bytes(sm_count);
+        return SEG_OK;
+    }
     if (F == 1) {
         // the scalar kernel: SW_NW warp units per CTA, each at least two chunks of
         // rows; a segment end weighs SW_CW rows in the partition

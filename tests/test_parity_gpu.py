@@ -323,3 +323,30 @@ def test_calls_with_changing_grids_share_scratch():
         for off, v in layouts:
             for op in ("sum", "max"):
                 _check(v, off, op, where=(off.size, op))
+
+
+@pytest.mark.parametrize("kind", ["f32", "u32", "s32"])
+def test_small_input_shape(kind):
+    """F == 1 inputs of at most 16,384 rows and 4,096 segments take the
+    one-CTA shape: short segments by a thread, longer ones by a warp.  Both
+    sides of both limits, segments of 32 and 33 rows (the thread / warp
+    split), long segments with many ties, empties, a non-zero first offset,
+    uint32 offsets; every output and arg against the oracle."""
+    import segmented_reduction_csr_gb300 as sr
+    rng = np.random.default_rng(zlib.crc32(f"small-{kind}".encode()))
+    layouts = []
+    for n, s in ((16_384, 4_096), (16_385, 4_096), (16_384, 4_097), (3_000, 200), (1, 1)):
+        cuts = np.sort(rng.integers(0, n + 1, size=s - 1))
+        off = np.concatenate([[0], cuts, [n]]).astype(np.int64)
+        layouts.append((n, off))
+    lengths = np.array([32, 33, 0, 31, 1, 5_000, 64, 0, 2_000, 97])
+    off = W.offsets_from_lengths(lengths)
+    layouts.append((int(off[-1]), off))
+    layouts.append((9_000, np.array([17, 17, 40, 2_000, 2_001, 8_000], np.int64)))   # o0 > 0, tail unreduced
+    for n, off in layouts:
+        v = _values(rng, n, kind, ties=True)
+        small = sr.plan(kind, 1, n, "i64", off.size - 1, "sum")["kernel_variant"] == 8
+        assert small == (n <= 16_384 and off.size - 1 <= 4_096)
+        for odt in (np.int64, np.uint32):
+            for op in _ops(kind):
+                _check(v, off.astype(odt), op, where=(kind, n, off.size, odt.__name__, op))
