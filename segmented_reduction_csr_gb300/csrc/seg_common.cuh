@@ -49,11 +49,17 @@ struct Params {
     uint32_t gen;                    // call generation, > 0, increasing per scratch buffer
 };
 
-// One cross-CTA partial: a float sum in double, an integer sum, or a
-// (value, absolute row) pair.
+// One cross-CTA partial: a float sum as a compensated pair (hi, lo), an
+// integer sum, or a (value, absolute row) pair.  No double arithmetic: FP64
+// issues far slower than FP32 on this part, and a combine over hundreds of
+// partials sat on the critical path.
+struct PartPair {
+    float hi, lo;
+};
 struct PartElem {
     union {
-        double d;
+        unsigned long long w;   // the raw 8 bytes (copies and shuffles)
+        PartPair c;
         uint32_t u;
         int32_t i;
         float f;
@@ -186,16 +192,24 @@ __device__ __forceinline__ void finish_carry(const CarryF2& c, int64_t len, int 
 }
 __device__ __forceinline__ PartElem to_part(const CarryF2& c) {
     PartElem p;
-    p.v.d = static_cast<double>(c.hi) + static_cast<double>(c.lo);
+    p.v.c = PartPair{c.hi, c.lo};
     p.row = -1;
     return p;
+}
+// (a.hi + a.lo) + (b.hi + b.lo) as a pair: TwoSum of the high parts, the
+// rounding error and both low parts carried in lo.
+__device__ __forceinline__ PartPair pair_add(const PartPair& a, const PartPair& b) {
+    const float s = a.hi + b.hi;
+    const float bb = s - a.hi;
+    const float err = (a.hi - (s - bb)) + (b.hi - bb);
+    return PartPair{s, (a.lo + b.lo) + err};
 }
 template <class T, int OP>
 __device__ __forceinline__ PartElem part_comb(const PartElem& e, const PartElem& l) {
     PartElem r;
     if constexpr (OP == OP_SUM) {
         if constexpr (kIsFloat<T>) {
-            r.v.d = e.v.d + l.v.d;
+            r.v.c = pair_add(e.v.c, l.v.c);
         } else {
             r.v.u = e.v.u + l.v.u;
         }
@@ -212,7 +226,7 @@ __device__ __forceinline__ void finish_part(const PartElem& p, int64_t len, int 
                                             int64_t& arg) {
     if constexpr (OP == OP_SUM) {
         if constexpr (kIsFloat<T>) {
-            const float f = static_cast<float>(p.v.d);
+            const float f = p.v.c.hi + p.v.c.lo;
             v = mean ? (len > 0 ? f / static_cast<float>(len) : 0.0f) : f;
         } else {
             v = from_bits<T>(p.v.u);
@@ -346,10 +360,10 @@ __device__ __forceinline__ bool ticket_last(unsigned long long old, uint32_t gen
 }
 
 __device__ __forceinline__ PartElem load_part(const PartElem* src) {
-    const double2 raw = __ldcg(reinterpret_cast<const double2*>(src));
+    const longlong2 raw = __ldcg(reinterpret_cast<const longlong2*>(src));
     PartElem pe;
-    pe.v.d = raw.x;
-    pe.row = __double_as_longlong(raw.y);
+    pe.v.w = static_cast<unsigned long long>(raw.x);
+    pe.row = raw.y;
     return pe;
 }
 

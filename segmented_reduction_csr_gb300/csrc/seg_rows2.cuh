@@ -82,12 +82,12 @@ __device__ __forceinline__ void rows_combine_store(const Params& p, const uint32
     const int F = p.F;
     const int c0 = slice * SLW + lane * VEC;
     if (c0 >= F) return;
-    double ds[VEC];
+    CarryF2 ds[VEC];   // float sums: a compensated pair (no FP64, which issues far slower)
     T tv[VEC];
     int64_t trow[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) {
-        ds[v] = 0.0;
+        ds[v] = CarryF2{0.0f, 0.0f};
         tv[v] = T(0);
         trow[v] = -1;
     }
@@ -115,7 +115,7 @@ __device__ __forceinline__ void rows_combine_store(const Params& p, const uint32
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) {
                     if constexpr (OP == OP_SUM) {
-                        if constexpr (kIsFloat<T>) ds[v] += static_cast<double>(__uint_as_float(b[j][v]));
+                        if constexpr (kIsFloat<T>) ds[v] = two_sum_add(ds[v], __uint_as_float(b[j][v]));
                         else tv[v] = add_wrap(tv[v], from_bits<T>(b[j][v]));
                     } else {
                         const T x = from_bits<T>(b[j][v]);
@@ -134,7 +134,7 @@ __device__ __forceinline__ void rows_combine_store(const Params& p, const uint32
     for (int v = 0; v < VEC; ++v) {
         T r;
         if constexpr (OP == OP_SUM && kIsFloat<T>) {
-            const float f = static_cast<float>(ds[v]);
+            const float f = ds[v].hi + ds[v].lo;
             r = p.mean ? (len > 0 ? f / static_cast<float>(len) : 0.0f) : f;
         } else {
             r = (OP != OP_SUM && trow[v] < 0) ? T(0) : tv[v];

@@ -98,7 +98,7 @@ __device__ __forceinline__ void warp_combine_store(const Params& p, const PartEl
     const int n = qc - pc + 1;
     const int per = (n + 31) / 32;
     PartElem a;
-    a.v.d = 0.0;
+    a.v.w = 0ull;
     a.row = -1;
     bool have = false;
     for (int t = 0; t < per; ++t) {
@@ -112,7 +112,7 @@ __device__ __forceinline__ void warp_combine_store(const Params& p, const PartEl
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         PartElem b;
-        b.v.d = __longlong_as_double(__shfl_down_sync(0xffffffffu, __double_as_longlong(a.v.d), o));
+        b.v.w = __shfl_down_sync(0xffffffffu, a.v.w, o);
         b.row = __shfl_down_sync(0xffffffffu, a.row, o);
         const bool bh = __shfl_down_sync(0xffffffffu, have, o);
         if ((lane & (2 * o - 1)) == 0 && bh) {
