@@ -85,7 +85,8 @@ seg_status_t plan_launch(seg_dtype_t dtype, int64_t F, int64_t num_values,
     else if (F % 4 == 0 && values_addr % 16 == 0 && F >= 128) vec = 4;
     else if (F % 2 == 0 && values_addr % 8 == 0 && F >= 64) vec = 2;
     const int64_t nsl = ceil_div(F, int64_t(32) * vec);           // column slices
-    const int64_t witems = num_values + int64_t(RW_CW) * S;
+    const int64_t cw = (op == SEG_MIN || op == SEG_MAX) ? RW_CW_ARG : RW_CW_SUM;   // as the kernel, args assumed
+    const int64_t witems = num_values + cw * S;
     const int64_t ranges = std::max<int64_t>(1, ceil_div(witems, RW_MIN_ITEMS));
     int64_t grid = ceil_div(ranges * nsl, RW_NW);
     grid = std::max<int64_t>(grid, ceil_div(nsl, RW_NW));           // every slice gets a unit

@@ -4,8 +4,8 @@
 //
 // Work split.  The columns are cut into slices of 32 * VEC (one VEC-wide
 // vector per lane), and for every slice the merged sequence of rows and
-// segment ends (a row weighs 1, an end RW_CW) is cut into ranges of equal
-// weight.  A warp owns one (slice, range) unit; one CTA of RW_NW warps per
+// segment ends (a row weighs 1, an end RW_CW_SUM, or RW_CW_ARG when it also
+// stores int64 rows) is cut into ranges of equal weight.  A warp owns one (slice, range) unit; one CTA of RW_NW warps per
 // SM.  A CTA finds the range boundaries its warps need with one cooperative
 // search (the same weighted merge-path search as the scalar kernel).
 //
@@ -30,7 +30,11 @@ namespace segred {
 
 constexpr int RW_NW = 8;                      // warps (units) per CTA
 constexpr int RW_NTHREADS = RW_NW * 32;
-constexpr int RW_CW = 2;                      // merge-path weight of a segment end, in rows
+// Merge-path weight of a segment end, in rows.  Measured on 10M x 128 f32
+// with evenly spaced ends: an end costs about 1.9 rows of time for a sum and
+// about 5 for a max that also stores its int64 rows (three times the bytes).
+constexpr int RW_CW_SUM = 2;
+constexpr int RW_CW_ARG = 5;
 constexpr int RW_NDIAG = RW_NW + 1;           // range boundaries per CTA (at most)
 constexpr int RW_GRID = 1024;                 // first-round probes, shared by all CTAs
 constexpr int RW_PROBES = 56;                 // later-round probes per boundary
@@ -70,6 +74,38 @@ __device__ __forceinline__ void ld_stream(uint32_t (&x)[VEC], const uint32_t* p,
                      : "=r"(x[0])
                      : "l"(p), "l"(pol));
     }
+}
+
+// A lane's VEC output columns: one vector store when `vec` (the caller
+// checked alignment), else one store per column.
+template <int VEC>
+__device__ __forceinline__ void store_cols(uint32_t* dst, const uint32_t (&r)[VEC], bool vec) {
+    if constexpr (VEC == 4) {
+        if (vec) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(r[0], r[1], r[2], r[3]);
+            return;
+        }
+    } else if constexpr (VEC == 2) {
+        if (vec) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(r[0], r[1]);
+            return;
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) dst[v] = r[v];
+}
+template <int VEC>
+__device__ __forceinline__ void store_args(int64_t* dst, const int64_t (&a)[VEC], bool vec) {
+    if constexpr (VEC >= 2) {
+        if (vec) {
+#pragma unroll
+            for (int v = 0; v < VEC; v += 2)
+                *reinterpret_cast<longlong2*>(dst + v) = make_longlong2(a[v], a[v + 1]);
+            return;
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) dst[v] = a[v];
 }
 
 // Last arriver of a segment that crosses ranges pc .. qc of slice `slice`:
@@ -162,6 +198,7 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     const int F = p.F;
     const int NSL = p.G;                               // column slices
     const int64_t U = static_cast<int64_t>(p.P) * RW_NW;
+    const int64_t CW = (OP != OP_SUM && p.out_arg != nullptr) ? RW_CW_ARG : RW_CW_SUM;
     const int64_t NR = U / NSL;                        // ranges per slice
     const OffT* offs = static_cast<const OffT*>(p.offsets);
 
@@ -174,9 +211,9 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     const int nb = static_cast<int>(rg_hi - rg_lo) + 2;   // boundaries rg_lo .. rg_hi + 1
 
     // ---- range boundaries: weighted merge path ---------------------------------
-    // End s sits at key(s) = (offsets[s+1] - o0) + RW_CW s; a cut at D takes
+    // End s sits at key(s) = (offsets[s+1] - o0) + CW s; a cut at D takes
     // the I(D) = #{s : key(s) < D} ends before it and the rows before both
-    // D - RW_CW I and the start of segment I.
+    // D - CW I and the start of segment I.
     // A small offsets array (staged shapes) is copied whole into shared
     // memory and each boundary is a binary search there: no probe rounds.
     RowsSearchSmem* ss = reinterpret_cast<RowsSearchSmem*>(smem);
@@ -200,19 +237,19 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     const int64_t oS_raw = small ? clamp_off(soffs[S], N) : ss->oS;
     const int64_t oS = oS_raw < o0 ? o0 : oS_raw;
     const int64_t nrows = oS - o0;
-    const int64_t total = nrows + RW_CW * S;
+    const int64_t total = nrows + CW * S;
     const int64_t Wr = (total + NR - 1) / NR;
     if (tid < nb) {
         const int64_t rg = rg_lo + tid;
         const int64_t D = rg * Wr < total ? rg * Wr : total;
-        int64_t lo = D > nrows ? (D - nrows + RW_CW - 1) / RW_CW : 0;
-        int64_t hi = (D + RW_CW - 1) / RW_CW;
+        int64_t lo = D > nrows ? (D - nrows + CW - 1) / CW : 0;
+        int64_t hi = (D + CW - 1) / CW;
         hi = hi < S ? hi : S;
         if (small) {
             // I = #{s : key(s) < D}: the first s in [lo, hi) with key(s) >= D
             while (lo < hi) {
                 const int64_t mid = (lo + hi) >> 1;
-                if (clamp_off(soffs[mid + 1], N) - o0 + RW_CW * mid < D)
+                if (clamp_off(soffs[mid + 1], N) - o0 + CW * mid < D)
                     lo = mid + 1;
                 else
                     hi = mid;
@@ -223,7 +260,7 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
             while (a < b) {
                 const int mid = (a + b) >> 1;
                 const int64_t sm = static_cast<int64_t>(mid) * S / RW_GRID;
-                if (ss->graw[mid] - o0 + RW_CW * sm < D)
+                if (ss->graw[mid] - o0 + CW * sm < D)
                     a = mid + 1;
                 else
                     b = mid;
@@ -252,7 +289,7 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
                 if (len > 0) {
                     const int64_t step = (len + RW_PROBES - 1) / RW_PROBES;
                     const int64_t s = lo + mm * step;
-                    if (s < hi && clamp_off(__ldg(&offs[s + 1]), N) - o0 + RW_CW * s < ss->D[k])
+                    if (s < hi && clamp_off(__ldg(&offs[s + 1]), N) - o0 + CW * s < ss->D[k])
                         atomicAdd(&ss->cnt[k], 1);
                 }
             }
@@ -283,7 +320,7 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     if (tid < nb) {
         const int64_t I = ss->lo[tid];
         const int64_t oI = I > 0 ? clamp_off(small ? soffs[I] : __ldg(&offs[I]), N) - o0 : 0;
-        int64_t R = ss->D[tid] - RW_CW * I;
+        int64_t R = ss->D[tid] - CW * I;
         R = R < oI ? oI : R;
         R = R < 0 ? 0 : (R > nrows ? nrows : R);
         ss->R[tid] = o0 + R;
@@ -321,10 +358,10 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     }
     bool adopt_head = false, give_tail = false;
     if (Iu < Iu2 && off_Iu < Rc && Rc - off_Iu <= RW_ADOPT && rg > 0)
-        adopt_head = (off_Iu - o0 + RW_CW * Iu) / Wr == rg - 1;
+        adopt_head = (off_Iu - o0 + CW * Iu) / Wr == rg - 1;
     if (Iu2 < S && off_Iu2 < Rc2 && Rc2 - off_Iu2 <= RW_ADOPT) {
-        const int64_t f = off_Iu2 - o0 + RW_CW * Iu2;
-        const int64_t e = (off_Iu21 > off_Iu2 ? off_Iu21 : off_Iu2) - o0 + RW_CW * Iu2;
+        const int64_t f = off_Iu2 - o0 + CW * Iu2;
+        const int64_t e = (off_Iu21 > off_Iu2 ? off_Iu21 : off_Iu2) - o0 + CW * Iu2;
         give_tail = f / Wr == rg && e / Wr == rg + 1;
     }
     const int64_t Ru = adopt_head ? off_Iu : Rc;
@@ -341,6 +378,10 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
     int64_t* pr = reinterpret_cast<int64_t*>(pv + 2 * U * SLW);     // [2U][SLW] partial rows
     const int mean = p.mean;
     const bool want_arg = (OP != OP_SUM) && p.out_arg != nullptr;
+    // one VEC-wide store per lane where the output rows allow it (every
+    // lane's first column is then a multiple of VEC)
+    const bool vec_out = VEC > 1 && F % VEC == 0 && reinterpret_cast<uintptr_t>(p.out) % (4 * VEC) == 0;
+    const bool vec_arg = VEC > 1 && F % 2 == 0 && reinterpret_cast<uintptr_t>(p.out_arg) % 16 == 0;
 
     // register ring: xb[d] holds row r0 + d
     uint32_t xb[PD][VEC];
@@ -417,23 +458,24 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
             head_pending = false;
         } else if (active) {
             const int32_t len = e > bst ? e - bst : 0;
+            uint32_t r[VEC];
+            int64_t a[VEC];
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                T r;
-                int64_t a = -1;
+                a[v] = -1;
                 if constexpr (kFloatSum) {
                     const CarryF2 c = two_sum_add(car[v], blk[v]);
                     const float f = c.hi + c.lo;
-                    r = mean ? (len > 0 ? f / static_cast<float>(len) : 0.0f) : f;
+                    r[v] = __float_as_uint(mean ? (len > 0 ? f / static_cast<float>(len) : 0.0f) : f);
                 } else if constexpr (OP == OP_SUM) {
-                    r = acc[v];
+                    r[v] = bits_of(acc[v]);
                 } else {
-                    r = arow[v] >= 0 ? acc[v] : T(0);
-                    a = arow[v] >= 0 ? Ru + arow[v] : -1;
+                    r[v] = bits_of(arow[v] >= 0 ? acc[v] : T(0));
+                    a[v] = arow[v] >= 0 ? Ru + arow[v] : -1;
                 }
-                out[s * F + c0 + v] = r;
-                if (want_arg) p.out_arg[s * F + c0 + v] = a;
             }
+            store_cols<VEC>(reinterpret_cast<uint32_t*>(out) + s * F + c0, r, vec_out);
+            if (want_arg) store_args<VEC>(p.out_arg + s * F + c0, a, vec_arg);
         }
         reset();
         bst = e;
@@ -639,8 +681,8 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
             __syncwarp();   // every lane's partial is out before the ticket
             if (lane == 0) {
                 const int64_t oe = off_Iu21;
-                const int64_t f = tob - o0 + RW_CW * Iu2;
-                const int64_t e = (oe > tob ? oe : tob) - o0 + RW_CW * Iu2;
+                const int64_t f = tob - o0 + CW * Iu2;
+                const int64_t e = (oe > tob ? oe : tob) - o0 + CW * Iu2;
                 tpc = f / Wr;
                 tqc = e / Wr;
                 tpc = tpc < 0 ? 0 : (tpc > rg ? rg : tpc);
@@ -653,7 +695,7 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
         }
     }
     if (head_taken) {
-        int64_t pc = (off_Iu - o0 + RW_CW * Iu) / Wr;
+        int64_t pc = (off_Iu - o0 + CW * Iu) / Wr;
         pc = pc < 0 ? 0 : (pc > rg ? rg : pc);
         const bool last =
             __shfl_sync(FULL, lane == 0 && ticket_last(head_ticket, p.gen, static_cast<int>(rg - pc + 1)), 0);
