@@ -244,7 +244,10 @@ seg_status_t seg_scan(const void *values, seg_dtype_t dtype, int64_t num_values,
  * scatter_mean (an output that receives no row is 0), scatter_max /
  * scatter_min returning (values, arg); index is [N] int64.  "Method": one
  * atomic per element; for max / min the value and its row settle inside one
- * 64-bit atomic, with ties to the lower row.
+ * 64-bit atomic, with ties to the lower row.  Here max / min first read the
+ * output's current word and skip the atomic when the element cannot win
+ * (the word only moves one way, so a stale read only costs an atomic); the
+ * results are those of one atomic per element.
  *
  *   src        device, [num_rows, F] row-major, element type `dtype`, aligned
  *              to 4 bytes (16 bytes, with out 16-byte aligned and F % 4 == 0,

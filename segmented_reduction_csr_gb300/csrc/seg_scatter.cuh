@@ -3,15 +3,18 @@
 // it there, max / min keep the extreme and the lowest row that holds it.
 //
 // One atomic per element (per four elements for float32 sums with 128-bit
-// vector reductions), as the page's method.  For max and min the value and
-// its row settle inside one 64-bit atomic: the value's bits made monotone
+// vector reductions), as the page's method, except that max and min skip
+// the atomic of an element that the output's current word already beats
+// (read from L2 just before; about ln n of n random candidates win).  For
+// max and min the value and its row settle inside one 64-bit atomic: the value's bits made monotone
 // (float32: negative values complemented, others with the sign bit set;
 // int32: the sign bit flipped; uint32: as is) in the high half, and the row
 // in the low half -- complemented for max, so that the largest word holds
 // the maximum and, among equal values, the lowest row; as is for min.
 // -0.0 is taken as +0.0 there (IEEE compares them equal, so the lower row
-// must win); the finishing pass reads the winning row's own value back
-// from src, so the output keeps its bits.
+// must win); the finishing pass turns the word's high half back into the
+// value, and reads a float32 zero back from the winning row of src, so the
+// output keeps its sign bit.
 //
 // Float32 sums and means are not deterministic: the order in which the
 // atomics land varies from run to run.  Integer sums (modulo 2^32) and max /
