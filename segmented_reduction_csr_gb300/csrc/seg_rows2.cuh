@@ -517,6 +517,21 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
             }
         }
     };
+    // the same once the segment has a row (min / max: no "first row" test,
+    // one compare and two selects per element)
+    auto add_row_seen = [&](const uint32_t (&x)[VEC], int32_t r) {
+        if constexpr (OP == OP_SUM) {
+            add_row(x, r);
+        } else {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const T xv = from_bits<T>(x[v]);
+                const bool better = (OP == OP_MIN) ? (xv < acc[v]) : (xv > acc[v]);
+                acc[v] = better ? xv : acc[v];
+                arow[v] = better ? r : arow[v];
+            }
+        }
+    };
     // register ring: row r is the value loaded PD rows ago; then load row r + PD
     auto take_row = [&](int d, int32_t r) {
         uint32_t x[VEC];
@@ -574,9 +589,8 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
             const int32_t rb = static_cast<int32_t>(k * RPC);
             const int32_t re = rb + RPC < nR ? rb + RPC : nR;
             const unsigned char* st = ring + (k % RW_NSR) * RW_CB + lane * VEC * 4;   // row rb, my columns
-            auto srow = [&](int32_t r) {
+            auto lrow = [&](int32_t r, uint32_t (&x)[VEC]) {
                 const unsigned char* q = st + static_cast<uint32_t>(r - rb) * rowb;
-                uint32_t x[VEC];
                 if constexpr (VEC == 4) {
                     const uint4 w = *reinterpret_cast<const uint4*>(q);
                     x[0] = w.x, x[1] = w.y, x[2] = w.z, x[3] = w.w;
@@ -586,14 +600,26 @@ __global__ void __launch_bounds__(RW_NTHREADS, 1) seg_rows2_kernel(const Params 
                 } else {
                     x[0] = *reinterpret_cast<const uint32_t*>(q);
                 }
+            };
+            auto srow = [&](int32_t r) {
+                uint32_t x[VEC];
+                lrow(r, x);
                 add_row(x, r);
             };
             for (int32_t r1 = rb; r1 < re; r1 += 32) {
                 const int32_t r2 = r1 + 32 < re ? r1 + 32 : re;
                 if (ecur >= r2 || s >= Iu2) {
                     if (active) {
+                        // no segment ends in these rows: after the segment's
+                        // first row (all lanes alike) the plain compare suffices
+                        int32_t r = r1;
+                        if (OP != OP_SUM && arow[0] < 0) srow(r++);
 #pragma unroll 8
-                        for (int32_t r = r1; r < r2; ++r) srow(r);
+                        for (; r < r2; ++r) {
+                            uint32_t x[VEC];
+                            lrow(r, x);
+                            add_row_seen(x, r);
+                        }
                     }
                 } else {
 #pragma unroll 2
