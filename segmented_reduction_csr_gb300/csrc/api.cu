@@ -169,7 +169,7 @@ seg_status_t fixed_state(int dev, cudaStream_t stream, FixedState** out) {
 
 // The offsets producers (run-length encoding, flags to offsets): the CTA
 // count, scratch from the (device, stream) buffer past the ticket words
-// (which these launches never touch), then the three launches.
+// (which these launches never touch), then the two launches.
 seg_status_t run_producer(RleParams& p, int64_t n, int64_t* count, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SEG_ERR_CUDA;
@@ -180,7 +180,7 @@ seg_status_t run_producer(RleParams& p, int64_t n, int64_t* count, cudaStream_t 
     p.n = n;
     p.count = count;
     p.tiles = ceil_div(n, RLE_TILE);
-    if (p.tiles > int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;   // one write CTA per tile
+    if (p.tiles > int64_t(INT32_MAX)) return SEG_ERR_UNSUPPORTED;   // tile indices stay 32-bit
     p.ctas = static_cast<int32_t>(std::min<int64_t>(
         p.tiles, std::min<int64_t>(int64_t(ds->sm_count) * RLE_CTAS_PER_SM, RLE_MAX_CTAS)));
     // scratch past the reduction's ticket words (which these launches never
@@ -190,17 +190,10 @@ seg_status_t run_producer(RleParams& p, int64_t n, int64_t* count, cudaStream_t 
     st = scratch_for(dev, stream,
                      static_cast<size_t>(ticket_bytes + RLE_CTA_SCRATCH + rle_tile_bytes(p.tiles)), &sc);
     if (st != SEG_OK) return st;
-    // the producers' ticket is slot 0 of the ticket words, tagged with a new
-    // generation like any reduction call on this scratch
-    sc->gen += 1;
-    p.gen = sc->gen;
-    p.ticket = static_cast<unsigned long long*>(sc->ptr);
     int64_t* ws = reinterpret_cast<int64_t*>(static_cast<unsigned char*>(sc->ptr) + ticket_bytes);
     p.cta_count = ws;
     p.cta_first = ws + RLE_MAX_CTAS;
-    p.cta_base = ws + 2 * RLE_MAX_CTAS;
-    p.cta_next = ws + 3 * RLE_MAX_CTAS;
-    p.tile_first = ws + 4 * RLE_MAX_CTAS;
+    p.tile_first = ws + 2 * RLE_MAX_CTAS;
     p.tile_count = reinterpret_cast<int32_t*>(p.tile_first + p.tiles);
     p.bitmap = reinterpret_cast<unsigned long long*>(
         reinterpret_cast<unsigned char*>(p.tile_first) + ((p.tiles * 12 + 255) / 256) * 256);

@@ -97,66 +97,6 @@ __device__ __forceinline__ void cta_tiles(const RleParams& p, int64_t& t0, int64
     t1 = p.tiles * (blockIdx.x + 1) / p.ctas;
 }
 
-// Run by the last count CTA: every CTA's first run index (exclusive sum of
-// the counts) and the first start after its range (suffix minimum of the
-// first starts, capped at n); the run count and offsets[count] = n.  Thread
-// i handles CTAs 4 i .. 4 i + 3.
-__device__ __forceinline__ void scan_ctas(const RleParams& p) {
-    constexpr int PER = RLE_MAX_CTAS / RLE_NT;
-    __shared__ int64_t s_sum[kWarps];
-    __shared__ int64_t s_min[kWarps];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int64_t c[PER], f[PER];
-    int64_t mine = 0, low = kNone;
-#pragma unroll
-    for (int k = 0; k < PER; ++k) {
-        const int i = threadIdx.x * PER + k;
-        c[k] = i < p.ctas ? __ldcg(p.cta_count + i) : 0;
-        f[k] = i < p.ctas ? __ldcg(p.cta_first + i) : kNone;
-        mine += c[k];
-        low = f[k] < low ? f[k] : low;
-    }
-    // inclusive prefix sum and inclusive suffix minimum over the warp
-    int64_t inc = mine, suf = low;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
-        const int64_t z = __shfl_down_sync(0xffffffffu, suf, o);
-        if (lane + o < 32 && z < suf) suf = z;
-    }
-    if (lane == 31) s_sum[warp] = inc;
-    if (lane == 0) s_min[warp] = suf;
-    __syncthreads();
-    int64_t before = inc - mine, total = 0, after = kNone;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        before += w < warp ? s_sum[w] : 0;
-        total += s_sum[w];
-        if (w > warp && s_min[w] < after) after = s_min[w];
-    }
-    // the minimum over later lanes of my warp
-    int64_t later = __shfl_down_sync(0xffffffffu, suf, 1);
-    if (lane < 31 && later < after) after = later;
-    // my entries, last to first, for the suffix minimum
-#pragma unroll
-    for (int k = PER - 1; k >= 0; --k) {
-        const int i = threadIdx.x * PER + k;
-        int64_t run = before;
-#pragma unroll
-        for (int k2 = 0; k2 < k; ++k2) run += c[k2];
-        if (i < p.ctas) {
-            p.cta_base[i] = run;
-            p.cta_next[i] = after < p.n ? after : p.n;
-        }
-        after = f[k] < after ? f[k] : after;
-    }
-    if (threadIdx.x == 0) {
-        *p.count = total;
-        if (p.offsets != nullptr) p.offsets[total] = p.n;
-    }
-}
-
 template <bool FLAGS>
 __global__ void __launch_bounds__(RLE_NT) rle_count_kernel(const RleParams p) {
     constexpr int PER = Raw<FLAGS>::PER;
@@ -217,17 +157,9 @@ __global__ void __launch_bounds__(RLE_NT) rle_count_kernel(const RleParams p) {
             tf = kNone;
         }
     }
-    __shared__ int s_last;
     if (threadIdx.x == 0) {
         p.cta_count[blockIdx.x] = cta_cnt;
         p.cta_first[blockIdx.x] = cta_first;
-        // the arrival releases the two words above
-        s_last = ticket_last(ticket_take(p.ticket, 0, p.gen), p.gen, p.ctas) ? 1 : 0;
-    }
-    __syncthreads();
-    if (s_last) {
-        fence_acq_rel_gpu();
-        scan_ctas(p);
     }
 }
 
@@ -253,39 +185,57 @@ __device__ __forceinline__ void owner_of(const RleParams& p, int64_t t, int64_t&
     }
 }
 
-// CTA t writes the runs that start in tile t.  Thread i owns bitmap word i:
-// elements tile0 + 64 i + [0, 64).  A tile without starts returns at once.
+// CTA t writes the runs that start in tile t (one CTA per tile lets the
+// hardware balance tiles dense in starts against empty ones).  Its first run
+// index is the counts of the count CTAs before its owner b plus those of b's
+// tiles before t; the first start after it is the earliest first start of
+// b's later tiles and of the later count CTAs.  Both come from one round of
+// loads, spread over the block, and a block-wide sum and minimum.  Thread i
+// owns bitmap word i (elements tile0 + 64 i + [0, 64)); a block scan ranks
+// the starts into shared memory, then offsets, values (a gather of
+// keys[start]) and lengths (the next start minus this one) go out
+// coalesced.  A tile without starts returns at once, except the last tile,
+// whose CTA writes the run count and offsets[count] = n.
 __global__ void __launch_bounds__(RLE_NT) rle_write_kernel(const RleParams p) {
     __shared__ uint16_t s_rel[RLE_TILE + 2 * (RLE_TILE / 64) + 2];
     __shared__ int s_warp[kWarps];
-    __shared__ int64_t s_run, s_next;
+    __shared__ int64_t s_sum[kWarps], s_min[kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = blockIdx.x;
+    const bool last_tile = t == p.tiles - 1;
+    const bool outputs = p.values != nullptr || p.lengths != nullptr || p.offsets != nullptr;
+    const int cnt = (outputs || last_tile) ? __ldcg(p.tile_count + t) : 0;
+    if (!last_tile && (!outputs || cnt == 0)) return;
     const int64_t tile0 = t * RLE_TILE;
-    if (__ldcg(p.tile_count + t) == 0) return;
-    const unsigned long long word = __ldcg(p.bitmap + t * RLE_NT + threadIdx.x);
-    if (warp == 0) {
-        int64_t b, t0, t1;
-        owner_of(p, t, b, t0, t1);
-        const int64_t b_run = __ldcg(p.cta_base + b), b_after = __ldcg(p.cta_next + b);
-        // runs before the tile: b's base plus the starts of b's tiles before t;
-        // the first start after the tile: in b's later tiles, else after b
-        int64_t runs = 0, nx = kNone;
-        for (int64_t i = t0 + lane; i < t; i += 32) runs += __ldcg(p.tile_count + i);
-        for (int64_t i = t + 1 + lane; i < t1; i += 32) {
+    const unsigned long long word = outputs ? __ldcg(p.bitmap + t * RLE_NT + threadIdx.x) : 0ull;
+    int64_t b, t0, t1;
+    owner_of(p, t, b, t0, t1);
+    int64_t before = 0, after = kNone;
+    for (int64_t i = threadIdx.x; i < p.ctas; i += RLE_NT) {
+        if (i < b) {
+            before += __ldcg(p.cta_count + i);
+        } else if (i > b) {
+            const int64_t f = __ldcg(p.cta_first + i);
+            after = f < after ? f : after;
+        }
+    }
+    for (int64_t i = t0 + threadIdx.x; i < t1; i += RLE_NT) {
+        if (i < t) {
+            before += __ldcg(p.tile_count + i);
+        } else if (i > t) {
             const int64_t f = __ldcg(p.tile_first + i);
-            nx = f < nx ? f : nx;
+            after = f < after ? f : after;
         }
+    }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            runs += __shfl_xor_sync(0xffffffffu, runs, o);
-            const int64_t f = __shfl_xor_sync(0xffffffffu, nx, o);
-            nx = f < nx ? f : nx;
-        }
-        if (lane == 0) {
-            s_run = b_run + runs;
-            s_next = nx < b_after ? nx : b_after;
-        }
+    for (int o = 16; o > 0; o >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+        const int64_t f = __shfl_xor_sync(0xffffffffu, after, o);
+        after = f < after ? f : after;
+    }
+    if (lane == 0) {
+        s_sum[warp] = before;
+        s_min[warp] = after;
     }
     // block exclusive sum of the start counts
     const int c = __popcll(word);
@@ -297,22 +247,30 @@ __global__ void __launch_bounds__(RLE_NT) rle_write_kernel(const RleParams p) {
     }
     if (lane == 31) s_warp[warp] = inc;
     __syncthreads();
+    int64_t run = 0, next = kNone;
     int slot = inc - c, total = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
+        run += s_sum[w];
+        next = s_min[w] < next ? s_min[w] : next;
         const int x = s_warp[w];
         slot += w < warp ? x : 0;
         total += x;
     }
+    next = next < p.n ? next : p.n;
+    if (last_tile && threadIdx.x == 0) {
+        *p.count = run + cnt;
+        if (p.offsets != nullptr) p.offsets[run + cnt] = p.n;
+    }
+    if (total == 0) return;
     // my starts, in order, into their slots
-    unsigned long long b = word;
-    while (b) {
-        const int j = __ffsll(static_cast<long long>(b)) - 1;
-        b &= b - 1;
+    unsigned long long bits = word;
+    while (bits) {
+        const int j = __ffsll(static_cast<long long>(bits)) - 1;
+        bits &= bits - 1;
         s_rel[rel_slot(slot++)] = static_cast<uint16_t>(threadIdx.x * 64 + j);
     }
     __syncthreads();
-    const int64_t run = s_run, next = s_next;
     const uint32_t* __restrict__ keys = p.keys;
     uint32_t* __restrict__ values = p.values;
     uint32_t* __restrict__ lengths = p.lengths;
@@ -344,11 +302,9 @@ cudaError_t launch_mode(const RleParams& p, cudaStream_t stream) {
     rle_count_kernel<FLAGS><<<p.ctas, RLE_NT, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (p.values != nullptr || p.lengths != nullptr || p.offsets != nullptr) {
-        rle_write_kernel<<<static_cast<unsigned>(p.tiles), RLE_NT, 0, stream>>>(p);
-        e = cudaGetLastError();
-    }
-    return e;
+    // the write pass also writes the count, so it runs even with no outputs
+    rle_write_kernel<<<static_cast<unsigned>(p.tiles), RLE_NT, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 template <class K>
