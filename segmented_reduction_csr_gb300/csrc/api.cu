@@ -672,7 +672,7 @@ seg_status_t seg_scan(const void* values, seg_dtype_t dtype, int64_t num_values,
     p.sm_count = ds->sm_count;
     p.gen = sc->gen;
     p.ticket = static_cast<unsigned long long*>(sc->ptr);
-    p.cta_aggf = reinterpret_cast<double*>(ws);
+    p.cta_aggf = reinterpret_cast<PartPair*>(ws);
     p.carryf = p.cta_aggf + RS_MAX_CTAS;
     p.cta_first = reinterpret_cast<int64_t*>(p.carryf + RS_MAX_CTAS);
     p.cta_aggi = reinterpret_cast<uint32_t*>(p.cta_first + RS_MAX_CTAS);

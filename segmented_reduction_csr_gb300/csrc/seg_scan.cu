@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(RS_NT, 8) rs_scan_kernel(const ScanParams p) {
     if (threadIdx.x == 0) {
         const int64_t rend = t1 * RS_TILE < p.N ? t1 * RS_TILE : p.N;
         p.cta_flag[blockIdx.x] = cf ? 1 : 0;
-        if constexpr (DT == 2 && OP == 0) p.cta_aggf[blockIdx.x] = static_cast<double>(cv);
+        if constexpr (DT == 2 && OP == 0) p.cta_aggf[blockIdx.x] = PartPair{cv, 0.0f};
         else p.cta_aggi[blockIdx.x] = to_word(cv);
         p.cta_first[blockIdx.x] = first < rend ? first : rend;
         // the arrival releases the words above
@@ -285,12 +285,22 @@ __global__ void __launch_bounds__(RS_NT, 8) rs_scan_kernel(const ScanParams p) {
     if (!s_last) return;
     fence_acq_rel_gpu();
     // the last CTA: each CTA's carry-in, a segmented exclusive scan of the
-    // aggregates (float32 sums in double); thread i takes CTAs 4 i .. 4 i + 3
+    // aggregates (float32 sums as compensated pairs: no FP64, which issues
+    // far slower than FP32 on this part); thread i takes CTAs PER i .. PER i + PER - 1
     constexpr int PER = RS_MAX_CTAS / RS_NT;
-    using A = typename std::conditional<DT == 2 && OP == 0, double, T>::type;
+    constexpr bool kPair = DT == 2 && OP == 0;
+    using A = typename std::conditional<kPair, PartPair, T>::type;
     __shared__ A s_av[kWarps];
     __shared__ int s_af[kWarps];
-    const A aid = static_cast<A>(id);
+    A aid;
+    if constexpr (kPair) aid = PartPair{0.0f, 0.0f};
+    else aid = id;
+    auto shfl_up_a = [&](A v, int o) -> A {
+        if constexpr (kPair)
+            return PartPair{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+        else
+            return __shfl_up_sync(0xffffffffu, v, o);
+    };
     bool af[PER];
     A av[PER];
     bool mf = false;
@@ -300,14 +310,17 @@ __global__ void __launch_bounds__(RS_NT, 8) rs_scan_kernel(const ScanParams p) {
         const int i = threadIdx.x * PER + k;
         af[k] = i < p.ctas && __ldcg(p.cta_flag + i) != 0;
         if (i < p.ctas) {
-            if constexpr (DT == 2 && OP == 0) av[k] = __ldcg(p.cta_aggf + i);
+            if constexpr (kPair) {
+                const float2 a = __ldcg(reinterpret_cast<const float2*>(p.cta_aggf + i));
+                av[k] = PartPair{a.x, a.y};
+            }
             else av[k] = from_word<T>(__ldcg(p.cta_aggi + i));
         } else {
             av[k] = aid;
         }
         bool f2 = af[k];
         A v2 = av[k];
-        if constexpr (DT == 2 && OP == 0) { v2 = f2 ? v2 : mv + v2; f2 = mf || f2; }
+        if constexpr (kPair) { v2 = f2 ? v2 : pair_add(mv, v2); f2 = mf || f2; }
         else combine<DT, OP>(mf, mv, f2, v2);
         mf = f2;
         mv = v2;
@@ -317,14 +330,14 @@ __global__ void __launch_bounds__(RS_NT, 8) rs_scan_kernel(const ScanParams p) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const bool f2 = __shfl_up_sync(0xffffffffu, f, o);
-        const A v2 = __shfl_up_sync(0xffffffffu, v, o);
+        const A v2 = shfl_up_a(v, o);
         if (lane >= o) {
-            if constexpr (DT == 2 && OP == 0) { v = f ? v : v2 + v; f = f2 || f; }
+            if constexpr (kPair) { v = f ? v : pair_add(v2, v); f = f2 || f; }
             else combine<DT, OP>(f2, v2, f, v);
         }
     }
     bool ef = __shfl_up_sync(0xffffffffu, f, 1);
-    A ev = __shfl_up_sync(0xffffffffu, v, 1);
+    A ev = shfl_up_a(v, 1);
     if (lane == 0) {
         ef = false;
         ev = aid;
@@ -339,23 +352,23 @@ __global__ void __launch_bounds__(RS_NT, 8) rs_scan_kernel(const ScanParams p) {
     for (int w = 0; w < warp; ++w) {
         bool f2 = s_af[w];
         A v2 = s_av[w];
-        if constexpr (DT == 2 && OP == 0) { v2 = f2 ? v2 : pv + v2; f2 = pf || f2; }
+        if constexpr (kPair) { v2 = f2 ? v2 : pair_add(pv, v2); f2 = pf || f2; }
         else combine<DT, OP>(pf, pv, f2, v2);
         pf = f2;
         pv = v2;
     }
-    if constexpr (DT == 2 && OP == 0) { ev = ef ? ev : pv + ev; ef = pf || ef; }
+    if constexpr (kPair) { ev = ef ? ev : pair_add(pv, ev); ef = pf || ef; }
     else combine<DT, OP>(pf, pv, ef, ev);
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
         const int i = threadIdx.x * PER + k;
         if (i < p.ctas) {
-            if constexpr (DT == 2 && OP == 0) p.carryf[i] = ev;
+            if constexpr (kPair) p.carryf[i] = ev;
             else p.carryi[i] = to_word(ev);
         }
         bool f2 = af[k];
         A v2 = av[k];
-        if constexpr (DT == 2 && OP == 0) { v2 = f2 ? v2 : ev + v2; f2 = ef || f2; }
+        if constexpr (kPair) { v2 = f2 ? v2 : pair_add(ev, v2); f2 = ef || f2; }
         else combine<DT, OP>(ef, ev, f2, v2);
         ef = f2;
         ev = v2;
@@ -381,9 +394,12 @@ __global__ void __launch_bounds__(RS_NT) rs_fix_kernel(const ScanParams p) {
     if (a >= e) return;
     T* out = static_cast<T*>(p.out);
     if constexpr (DT == 2 && OP == 0) {
-        const double c = __ldcg(p.carryf + b);
-        const float ch = static_cast<float>(c);
-        const float cl = static_cast<float>(c - static_cast<double>(ch));
+        // the carry as a normalised pair: ch = hi + lo rounded, cl what that
+        // rounding dropped, so that ch + (cl + x) rounds like one addition
+        const float2 c2 = __ldcg(reinterpret_cast<const float2*>(p.carryf + b));
+        const PartPair c{c2.x, c2.y};
+        const float ch = c.hi + c.lo;
+        const float cl = c.lo - (ch - c.hi);
         for (int64_t r = a + threadIdx.x; r < e; r += RS_NT) out[r] = __fadd_rn(ch, __fadd_rn(cl, out[r]));
     } else {
         const T c = from_word<T>(__ldcg(p.carryi + b));

@@ -15,8 +15,8 @@
 //     The CTA records its aggregate -- whether its range holds a start, and
 //     the reduction of its rows after the last start -- and the row of its
 //     first start.  The CTA that arrives last on a generation-tagged ticket
-//     scans the aggregates into each CTA's carry-in (float32 sums in
-//     double);
+//     scans the aggregates into each CTA's carry-in (float32 sums as
+//     compensated float pairs);
 //  4. fix-up: the rows of each range before its first start belong to a
 //     segment that began in an earlier range; they get the carry-in added
 //     (float32 sums as a two-float carry, so the rounding stays that of one
@@ -25,6 +25,8 @@
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
+
+#include "seg_common.cuh"   // PartPair
 
 namespace segred {
 
@@ -49,11 +51,11 @@ struct ScanParams {
     uint32_t gen;
     unsigned long long* ticket;
     unsigned long long* bitmap;   // scratch [N / 64 + 1]
-    double* cta_aggf;             // scratch [ctas]: float32 sums
+    PartPair* cta_aggf;           // scratch [ctas]: float32 sums (hi, lo)
     uint32_t* cta_aggi;           // scratch [ctas]: other ops (value bits)
     int32_t* cta_flag;            // scratch [ctas]: the range holds a start
     int64_t* cta_first;           // scratch [ctas]: first start row of the range (or its end)
-    double* carryf;               // scratch [ctas]
+    PartPair* carryf;             // scratch [ctas]
     uint32_t* carryi;             // scratch [ctas]
 };
 

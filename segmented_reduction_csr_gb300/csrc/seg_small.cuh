@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(SM_NT, 1) seg_small_kernel(const Params p) {
     constexpr unsigned FULL = 0xffffffffu;
     constexpr bool kFloatSum = OP == OP_SUM && kIsFloat<T>;
     constexpr int KO = (SM_MAXS + 1 + SM_NT - 1) / SM_NT;
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem[];   // aligned as the other kernels declare it
     OffT* sraw = reinterpret_cast<OffT*>(smem);                            // [S + 1] offsets as given
     int32_t* so = reinterpret_cast<int32_t*>(smem);                         // ... then clamped to [0, N]
     uint32_t* sv = reinterpret_cast<uint32_t*>(smem + (SM_MAXS + 1) * 8);  // rows [0, N)
