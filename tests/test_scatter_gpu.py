@@ -102,7 +102,36 @@ def test_misaligned_src_takes_scalar_reductions(sr):
     dv = base[1:].view(4001, 8)
     assert dv.data_ptr() % 16 != 0
     idx = rng.integers(0, 50, size=4001).astype(np.int64)
-    _check(sr, v, idx, 50, "sum", dv=dv, where="misaligned")
+    for op in ("sum", "min", "max"):   # min / max: one column an item
+        _check(sr, v, idx, 50, op, dv=dv, where="misaligned")
+
+
+@pytest.mark.parametrize("order", ["rising", "falling"])
+@pytest.mark.parametrize("kind", ["u32", "s32", "f32"])
+def test_extremes_along_monotone_rows(sr, order, kind):
+    """max / min skip an element's atomic when its output already holds a
+    better value.  Values that rise along the rows make every element of a
+    max improve on its output (each reaches its atomic) and nearly every
+    element of a min lose; falling values the reverse.  Runs of equal values
+    (ties, settled by the atomic: the lowest row wins) and the type's extreme
+    values are mixed in.  Both must give the one-atomic-per-element result."""
+    rng = np.random.default_rng(("rising", "falling").index(order) * 10 + ("u32", "s32", "f32").index(kind))
+    n, feat, dim = 60_000, 8, 37
+    v = np.sort(_values(rng, kind, (n, feat)), axis=0)
+    m = v[1::7].shape[0]
+    v[0::7][:m] = v[1::7]   # equal neighbours (the order stays monotone)
+    if kind == "s32":
+        v[:50] = np.iinfo(np.int32).min
+        v[-50:] = np.iinfo(np.int32).max
+    elif kind == "u32":
+        v[:50] = 0
+        v[-50:] = np.iinfo(np.uint32).max
+    if order == "falling":
+        v = v[::-1].copy()
+    idx = rng.integers(0, dim, size=n).astype(np.int64)
+    dv = to_dev(v)
+    for op in ("max", "min"):
+        _check(sr, v, idx, dim, op, dv=dv, where=f"{order} {kind}")
 
 
 def test_no_rows(sr):
