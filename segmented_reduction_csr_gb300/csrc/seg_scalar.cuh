@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     // ---- a2: unit boundaries ---------------------------------------------------
     // Weighted merge path: end s sits at key(s) = (offsets[s+1] - o0) + SW_CW s.
     // A cut at D takes the I(D) = #{s : key(s) < D} ends before it and the rows
-    // before both D - SW_CW I and the start of segment I.  Round 1 reads a
+    // before both D - SW_CW I and the start of segment I.  The first probe round reads a
     // fixed grid of SW_GRID keys that every CTA shares (so it hits L2); then
     // each boundary narrows its bracket with SW_PROBES probes per round.
     // A small offsets array is copied whole into shared memory and each
