@@ -533,14 +533,35 @@ def measure_config(args, w: W.Workload, dev, world: int, flush, headline: bool):
     return res
 
 
+def e2e_chunks(offsets: np.ndarray, row_bytes: int) -> list:
+    """Segment ranges [a, b) for the end-to-end step: about equal row counts,
+    cut at segment boundaries, one chunk per 512 MB of values (at most 8)."""
+    off = np.asarray(offsets, dtype=np.int64)
+    S = off.size - 1
+    g = int(min(8, max(1, row_bytes // (512 << 20))))
+    if S <= 0 or g == 1:
+        return [(0, S)]
+    o0, oS = int(off[0]), int(off[S])
+    cuts = {0, S}
+    for k in range(1, g):
+        cuts.add(int(np.searchsorted(off[:S], o0 + (oS - o0) * k // g, side="left")))
+    cuts = sorted(c for c in cuts if 0 <= c <= S)
+    return [(a, b) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+
+
 def _e2e(args, w, dev, world, stream, dvals, doff, outs, call, bytes_step):
     """The same bytes through host buffers: every step copies its inputs up
-    from pinned memory, runs the calls and copies every output back.  The
-    step is pipelined over three streams: the offsets and then each dtype's
-    values go up on a copy stream; a dtype's calls start on the compute
-    stream as soon as its values have arrived; its outputs go back on a
-    third stream while the next dtype computes."""
+    from pinned memory, runs the calls and copies every output back, over
+    three streams.  The offsets go up first.  Each dtype's values go up in
+    row chunks cut at segment boundaries (large inputs: one per 512 MB); the
+    segments of a chunk are reduced through the public call as soon as its
+    rows have arrived, and their outputs go back while later chunks still
+    travel.  After the timed steps the outputs on the host are compared with
+    the device-resident calls' (max / min bit for bit, sums within the
+    parity bar)."""
     import torch
+
+    import segmented_reduction_csr_gb300 as sr
     cases = cases_of(w)
     host_vals = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int32) if v.dtype == np.uint32 else v)).pin_memory()
                  for k, v in w.values.items()}
@@ -554,33 +575,48 @@ def _e2e(args, w, dev, world, stream, dvals, doff, outs, call, bytes_step):
     up = torch.cuda.Stream(dev)
     down = torch.cuda.Stream(dev)
     kinds = list(dict.fromkeys(k for k, _ in cases))
+    chunked = not (SCAN or SEQUENTIAL)
+    offs = np.asarray(w.offsets, dtype=np.int64)
+    row_bytes = max(t.numel() * t.element_size() for t in host_vals.values())
+    chunks = e2e_chunks(offs, row_bytes) if chunked else [(0, w.num_segments)]
+
+    def chunk_call(k, op, a, b):
+        o, ar = outs[(k, op)]
+        if chunked:
+            sr.seg_reduce(dvals[k], doff[a:b + 1], op, out=o[a:b], out_arg=ar[a:b] if ar is not None else None,
+                          with_arg=ar is not None)
+        else:
+            call(k, op)
 
     def e2e_step():
         up.wait_stream(stream)             # the previous step no longer reads the inputs
-        ready = {}
         with torch.cuda.stream(up):
             doff.copy_(host_off, non_blocking=True)
-            for k in kinds:
-                dst = dvals[k].view(torch.int32) if dvals[k].dtype == torch.uint32 else dvals[k]
-                dst.copy_(host_vals[k], non_blocking=True)
-                ready[k] = torch.cuda.Event()
-                ready[k].record(up)
         for k in kinds:
-            stream.wait_event(ready[k])
-            for kk, op in cases:
-                if kk == k:
-                    call(kk, op)
-            done = torch.cuda.Event()
-            done.record(stream)
-            down.wait_event(done)
-            with torch.cuda.stream(down):
-                for (kk, op), (ho, ha) in host_outs.items():
-                    if kk != k:
-                        continue
-                    o, a = outs[(kk, op)]
-                    ho.copy_(o.view(torch.int32) if o.dtype == torch.uint32 else o, non_blocking=True)
-                    if ha is not None:
-                        ha.copy_(a, non_blocking=True)
+            dst = dvals[k].view(torch.int32) if dvals[k].dtype == torch.uint32 else dvals[k]
+            for a, b in chunks:
+                r0, r1 = (int(offs[a]), int(offs[b])) if chunked else (0, dst.shape[0])
+                ready = torch.cuda.Event()
+                with torch.cuda.stream(up):
+                    if r1 > r0:
+                        dst[r0:r1].copy_(host_vals[k][r0:r1], non_blocking=True)
+                    ready.record(up)
+                stream.wait_event(ready)
+                for kk, op in cases:
+                    if kk == k:
+                        chunk_call(kk, op, a, b)
+                done = torch.cuda.Event()
+                done.record(stream)
+                down.wait_event(done)
+                with torch.cuda.stream(down):
+                    for (kk, op), (ho, ha) in host_outs.items():
+                        if kk != k:
+                            continue
+                        o, ar = outs[(kk, op)]
+                        src = o.view(torch.int32) if o.dtype == torch.uint32 else o
+                        ho[a:b].copy_(src[a:b], non_blocking=True)
+                        if ha is not None:
+                            ha[a:b].copy_(ar[a:b], non_blocking=True)
         stream.wait_stream(down)           # the step ends with its outputs on the host
 
     for _ in range(max(1, args.warmup)):
@@ -593,9 +629,30 @@ def _e2e(args, w, dev, world, stream, dvals, doff, outs, call, bytes_step):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    # the host outputs against one device-resident call of each case: max /
+    # min bit for bit, float sums and means within 1e-5 * (the mean or sum
+    # of |x|) + 1e-6, the parity bar (a chunk's partition differs)
+    match = True
+    if chunked:
+        for (k, op), (ho, ha) in host_outs.items():
+            call(k, op)
+            o, ar = outs[(k, op)]
+            got = ho.to(dev)
+            ref = o.view(torch.int32) if o.dtype == torch.uint32 else o
+            if op in ("min", "max") or ref.dtype != torch.float32:
+                match = match and torch.equal(got.view(torch.int32), ref.view(torch.int32))
+                if ha is not None:
+                    match = match and torch.equal(ha.to(dev), ar)
+            else:
+                absr = sr.seg_reduce(dvals[k].abs(), doff, "mean" if op == "mean" else "sum")
+                match = match and bool(((got - ref).abs() <= 1e-5 * absr + 1e-6).all())
+        torch.cuda.synchronize(dev)
     return {"value": whole_job_gbs(world, bytes_step, args.steps, e2e_ms), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipelined": "each dtype's values go up while the previous dtype computes; its outputs come back while the next computes"}
+            "pipelined": (f"offsets up first; each dtype's values up in {len(chunks)} row chunk(s) cut at segment "
+                          "boundaries, a chunk's segments reduced by the public call as soon as its rows arrive, "
+                          "their outputs back while later chunks travel"),
+            "outputs_match_device_calls": bool(match)}
 
 
 def run_ours(args, names):
