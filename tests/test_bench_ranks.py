@@ -113,3 +113,33 @@ def test_suite_headline_is_the_largest_workload():
     import bench
     assert bench.SUITE[0] == "large"
     assert set(bench.SUITE) == {"tiny", "bulk", "mp", "skewed", "large"}
+
+
+def test_end_to_end_chunks_cut_at_segment_boundaries():
+    """The end-to-end step's row chunks: every segment in exactly one chunk,
+    in order; about one chunk per 512 MB of values (at most 8); a segment
+    longer than a chunk is never cut; small inputs go up in one piece."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import workloads as W
+    w = W.make("large", with_values=False)
+    off = w.offsets.astype(np.int64)
+    ch = bench.e2e_chunks(off, 10_000_000 * 128 * 4)
+    assert ch[0][0] == 0 and ch[-1][1] == off.size - 1
+    assert all(a < b for a, b in ch) and all(ch[i][1] == ch[i + 1][0] for i in range(len(ch) - 1))
+    assert 2 <= len(ch) <= 8
+    rows = [int(off[b] - off[a]) for a, b in ch]
+    assert sum(rows) == int(off[-1] - off[0])
+    # the 5M-row segment sits whole in one chunk
+    g = int(np.argmax(np.diff(off)))
+    assert any(a <= g < b for a, b in ch)
+    # evenly spread segments give about equal chunks
+    even = np.arange(0, 8_000_001, 1000, dtype=np.int64)
+    ch2 = bench.e2e_chunks(even, 8 * (512 << 20))
+    assert len(ch2) == 8
+    r2 = [int(even[b] - even[a]) for a, b in ch2]
+    assert max(r2) - min(r2) <= 1000
+    # below 512 MB, or with no segment, one chunk
+    assert bench.e2e_chunks(even, 100 << 20) == [(0, even.size - 1)]
+    assert bench.e2e_chunks(np.zeros(1, np.int64), 1 << 40) == [(0, 0)]
