@@ -19,7 +19,8 @@ Beside the reduction (``seg_reduce``, ``segment_*_csr``, ``seg_reduce_noalloc``)
 * ``seg_reduce_sequential``: float32 sum / mean added in input order
   (bitwise equal to an in-order float32 loop, as torch.segment_reduce);
 * ``scatter`` / ``scatter_{sum,add,mean,max,min}``: the unsorted path, one
-  atomic per element (graph-reduce README "API");
+  atomic per element (graph-reduce README "API"; max / min skip the atomic
+  of an element its output already beats);
 * ``seg_scan`` / ``segment_cumsum_csr``: segmented inclusive / exclusive scan;
 * ``seg_rle`` / ``rle`` / ``unique`` and ``seg_flags_to_offsets`` /
   ``flags_to_offsets``: producers of offsets (GPURunLengthEncode, GPUUnique,
