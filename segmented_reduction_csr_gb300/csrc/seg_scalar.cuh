@@ -78,6 +78,7 @@ static_assert(SW_SMEM <= 227 * 1024, "one CTA per SM");
 struct SearchSmem {
     int64_t graw[SW_GRID];
     int64_t D[SW_NDIAG], lo[SW_NDIAG], hi[SW_NDIAG], R[SW_NDIAG];
+    int64_t oI[SW_NDIAG], oI1[SW_NDIAG];   // offsets[I], offsets[I + 1] of each cut (clamped)
     int cnt[SW_NDIAG];
     int64_t o0, oS;
 };
@@ -164,13 +165,15 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
         cp_async_commit();
         cp_async_wait_all();
     } else {
-        prefetch_offsets_slice(p.offsets, static_cast<uint64_t>(S + 1) * OSZ, cta, p.P, tid, SW_NTHREADS);
+        // the grid's loads go out first, then the L2 prefetch of this CTA's
+        // slice of the offsets (which the probe rounds and tiles read later)
         if (tid == 0) ss->o0 = clamp_off(__ldg(&offs[0]), N);
         if (tid == 1) ss->oS = clamp_off(__ldg(&offs[S]), N);
         for (int m = tid; m < SW_GRID; m += SW_NTHREADS) {
             const int64_t sm = static_cast<int64_t>(m) * S / SW_GRID;
             ss->graw[m] = clamp_off(__ldg(&offs[sm + 1]), N);
         }
+        prefetch_offsets_slice(p.offsets, static_cast<uint64_t>(S + 1) * OSZ, cta, p.P, tid, SW_NTHREADS);
     }
     __syncthreads();
     const int64_t o0 = small ? clamp_off(soffs[0], N) : ss->o0;
@@ -258,13 +261,19 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
         if (!__syncthreads_or(open)) break;
     }
     if (tid < SW_NDIAG) {
-        // rows before the cut: D - SW_CW I, but never fewer than segment I's start
+        // rows before the cut: D - SW_CW I, but never fewer than segment I's
+        // start; offsets[I] and offsets[I + 1] load together and stay for the
+        // warps' cut-crossing segments
         const int64_t I = ss->lo[tid];
-        const int64_t oI = I > 0 ? clamp_off(small ? soffs[I] : __ldg(&offs[I]), N) - o0 : 0;
+        const int64_t vI = clamp_off(small ? soffs[I] : __ldg(&offs[I]), N);
+        const int64_t vI1 = I < S ? clamp_off(small ? soffs[I + 1] : __ldg(&offs[I + 1]), N) : 0;
+        const int64_t oI = I > 0 ? vI - o0 : 0;
         int64_t R = ss->D[tid] - SW_CW * I;
         R = R < oI ? oI : R;
         R = R < 0 ? 0 : (R > nrows ? nrows : R);
         ss->R[tid] = o0 + R;
+        ss->oI[tid] = vI;
+        ss->oI1[tid] = vI1;
     }
     __syncthreads();
     // my unit: weighted positions [Dlo, Dhi), ends [Iu, Iu2), rows [Ru, Ru2)
@@ -275,22 +284,15 @@ __global__ void __launch_bounds__(SW_NTHREADS, 1) seg_scalar_kernel(const Params
     const int64_t Rc = ss->R[warp];                              // the cuts' rows
     const int64_t Rc2 = ss->R[warp + 1] > Rc ? ss->R[warp + 1] : Rc;
     // Offsets of the segment that crosses each cut (the head and tail logic
-    // needs them): from the shared copy while it lives, else loaded below.
-    int64_t off_Iu = 0, off_Iu1 = 0, off_Iu2 = 0, off_Iu21 = 0;
-    if (small) {
-        off_Iu = clamp_off(soffs[Iu], N);
-        off_Iu1 = Iu < S ? clamp_off(soffs[Iu + 1], N) : 0;
-        off_Iu2 = Iu2 < S ? clamp_off(soffs[Iu2], N) : 0;
-        off_Iu21 = Iu2 < S ? clamp_off(soffs[Iu2 + 1], N) : 0;
-    }
+    // needs them), as the search left them (Iu2 is cut warp + 1's I, or Iu
+    // itself when offsets decrease)
+    const int j2 = ss->lo[warp + 1] > Iu ? warp + 1 : warp;
+    const int64_t off_Iu = ss->oI[warp];
+    const int64_t off_Iu1 = Iu < S ? ss->oI1[warp] : 0;
+    const int64_t off_Iu2 = Iu2 < S ? ss->oI[j2] : 0;
+    const int64_t off_Iu21 = Iu2 < S ? ss->oI1[j2] : 0;
     __syncthreads();   // the search scratch is dead from here on
     if (Dlo >= Dhi) return;
-    if (!small) {
-        off_Iu = clamp_off(__ldg(&offs[Iu]), N);
-        off_Iu1 = Iu < S ? clamp_off(__ldg(&offs[Iu + 1]), N) : 0;
-        off_Iu2 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2]), N) : 0;
-        off_Iu21 = Iu2 < S ? clamp_off(__ldg(&offs[Iu2 + 1]), N) : 0;
-    }
     // A segment that crosses just one cut, with at most SW_ADOPT rows before
     // it, is adopted whole by the unit that holds its end: that unit starts
     // at the segment's first row and the unit before it stops there, so no
