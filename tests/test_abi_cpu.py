@@ -196,6 +196,20 @@ def test_plan_shapes(lib):
                 assert p["workspace_bytes"] >= 2 * units * 32 * p["vec"] * per
 
 
+def test_plan_weighs_ends_by_op_and_routes_small_calls(lib):
+    # rows kernel: an end weighs 2 rows for sums, 5 when min / max store rows,
+    # so the same small problem gets more ranges (a larger grid) for max
+    ps = sr.plan("f32", 64, 2000, "i64", 1000, "sum", values_addr=256, sm_count=152)
+    pm = sr.plan("f32", 64, 2000, "i64", 1000, "max", values_addr=256, sm_count=152)
+    assert ps["grid"] == 4 and pm["grid"] == 7            # ceil(ceil((2000 + w * 1000) / 128) / 8)
+    # F = 1 up to 16,384 rows and 4,096 segments: the one-CTA small-input kernel
+    small = sr.plan("f32", 1, 16_384, "i64", 4_096, "sum", sm_count=152)
+    assert small["grid"] == 1 and small["block"] == 1024 and small["kernel_variant"] == 8
+    for n, s in ((16_385, 4_096), (16_384, 4_097)):
+        big = sr.plan("f32", 1, n, "i64", s, "sum", sm_count=152)
+        assert big["kernel_variant"] == 4                  # the scalar kernel
+
+
 def test_plan_rejects(lib):
     with pytest.raises(sr.SegReduceError):
         sr.plan("s32", 1, 10, "i64", 2, "mean")
